@@ -1,0 +1,550 @@
+"""Benchmark of the weight-absorbed MLA decode path on one GB300.
+
+A step is one decode step of the large V3 workload: 64 sequences, 128 heads,
+context lengths drawn uniformly from [1024, 16384], page 64, random block
+table; bf16 storage, fp32 accumulation. One step runs every stage of the path
+through the C ABI: absorb (W_UK fold) -> q concat -> cache write of the new
+rows -> split-KV decode (schedule, split kernel, LSE combine) -> v_up (W_UV).
+Inputs are resident in HBM before the timed region; the latent cache (about
+0.56 GB) is larger than L2 (129 MB), so no flush is needed between steps.
+
+Printed (rank 0, one JSON line): value = latent-KV GB/s, i.e. the decode
+stage's algorithmic bytes (cache rows read, q_cat read, o_lat written, block
+table and lengths read) per step over the step time; queries/s beside it; the
+roofline of the decode call (timed live with CUDA events on its stream); the
+end-to-end figure through the same API with host buffers; the float64 oracle
+timed on a bounded sample on the host cores; and the SM clocks sampled during
+the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode latent-KV HBM GB/s (% roofline); queries/s at 128 heads"
+UNIT = "GB/s"
+WORKLOAD = "v3_bf16_decode_b64_ctx1k-16k"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# --------------------------------------------------------------------------- helpers
+
+def _peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS,
+                bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def decode_algorithmic_bytes(seq_lens, B, H, L, R, max_blocks, es=2) -> int:
+    """Bytes the decode stage must move: every cached row once, q_cat in, o_lat out,
+    the block-table entries in use and the lengths."""
+    E = L + R
+    rows = int(sum(int(n) for n in seq_lens))
+    pages = int(sum((int(n) + 63) // 64 for n in seq_lens))
+    return rows * E * es + B * H * E * es + B * H * L * es + pages * 4 + B * 4
+
+
+def decode_algorithmic_flops(seq_lens, H, L, R) -> int:
+    return int(sum(int(n) for n in seq_lens)) * H * 2 * ((L + R) + L)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        # the busiest samples are the ones under load
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _traffic_for(kernel_src: str) -> float | None:
+    """ncu DRAM bytes per launch recorded for the current source of the kernel, else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    entry = d.get("decode")
+    if not entry:
+        return None
+    src = open(os.path.join(ROOT, "mla_latent_kv_11_gb300", "csrc", kernel_src), "rb").read()
+    if hashlib.sha256(src).hexdigest()[:16] != entry.get("source_sha"):
+        return None
+    return float(entry["bytes_per_launch"])
+
+
+# --------------------------------------------------------------------------- the workload
+
+class DecodeStep:
+    """Device-resident inputs of one decode step and the five calls that run it."""
+
+    def __init__(self, mla, w, device, rank_seed=0):
+        import numpy as np
+        import torch
+        self.mla, self.w = mla, w
+        g = w.geom
+        self.B, self.H, self.P, self.R, self.V, self.L = w.batch, g.n_head, g.d_nope, g.d_rope, g.d_v, g.kv_rank
+        self.E = self.L + self.R
+        dt = torch.bfloat16
+
+        def dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(dt)
+
+        self.dev = dev
+        self.q_nope = dev(w.q_nope)
+        self.q_pe = dev(w.q_pe)
+        self.w_uk = dev(w.w_uk)
+        self.w_uv = dev(w.w_uv)
+        self.new_kv_c = dev(w.new_kv_c)
+        self.new_k_pe = dev(w.new_k_pe)
+        self.slots = torch.from_numpy(w.slots).to(device)
+        self.table = torch.from_numpy(w.block_table).to(device)
+        self.lens = torch.from_numpy(w.seq_lens).to(device)
+        self.cache = dev(w.full_cache())
+        B, H, L, E, V = self.B, self.H, self.L, self.E, self.V
+        self.q_lat = torch.empty((H, B, L), dtype=dt, device=device)
+        self.q_cat = torch.empty((B, H, E), dtype=dt, device=device)
+        self.o_lat = torch.empty((B, H, L), dtype=dt, device=device)
+        self.out = torch.empty((B, H, V), dtype=dt, device=device)
+        self.ws = torch.empty(mla.mla_decode_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
+        self.launches_per_step = 7
+
+    def run(self, ev_decode=None, q_nope=None, q_pe=None, kv_c=None, k_pe=None, slots=None,
+            table=None, lens=None):
+        m = self.mla
+        q_nope = self.q_nope if q_nope is None else q_nope
+        m.mla_absorb_q(self.q_lat, q_nope.transpose(0, 1), self.w_uk)
+        m.mla_concat_q(self.q_cat, self.q_lat.transpose(0, 1), self.q_pe if q_pe is None else q_pe)
+        m.mla_cache_write(self.cache, self.new_kv_c if kv_c is None else kv_c,
+                          self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
+        if ev_decode is not None:
+            ev_decode[0].record()
+        m.mla_decode(self.o_lat, self.q_cat, self.cache, self.table if table is None else table,
+                     self.lens if lens is None else lens, self.L, self.R, self.w.scale, workspace=self.ws)
+        if ev_decode is not None:
+            ev_decode[1].record()
+        m.mla_v_up(self.out.transpose(0, 1), self.o_lat.transpose(0, 1), self.w_uv)
+
+
+def _smi_id(local: int) -> str:
+    """nvidia-smi's name for torch device ``local`` (its UUID: CUDA_VISIBLE_DEVICES renumbers)."""
+    import torch
+    u = getattr(torch.cuda.get_device_properties(local), "uuid", None)
+    if u is None:
+        return str(local)
+    u = str(u)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
+def _dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, group=None) -> float:
+    """The maximum of a per-rank float over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, group=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(w, n_seq: int, start: int = 0):
+    """A bounded sample of the workload for the oracle: sequences [start, start+n_seq)
+    with their own blocks only (block ids renumbered), in float64."""
+    import numpy as np
+    import mla_inputs as mi
+    ids = [(start + i) % w.batch for i in range(n_seq)]
+    lens = w.seq_lens[ids]
+    page, E = w.page, w.geom.entry
+    need = [(int(n) + page - 1) // page for n in lens]
+    old_blocks = np.concatenate([w.block_table[b, :k] for b, k in zip(ids, need)])
+    table = np.zeros((n_seq, max(need)), np.int64)
+    k = 0
+    for i, n in enumerate(need):
+        table[i, :n] = np.arange(k, k + n)
+        k += n
+    storage = mi.decode_f64(w.cache_rows(old_blocks).reshape(-1), w.dtype)
+    # slots of the appended rows, renumbered into the sample's blocks
+    slots = np.array([table[i, (int(lens[i]) - 1) // page] * page + (int(lens[i]) - 1) % page
+                      for i in range(n_seq)], np.int64)
+    f = lambda a: mi.decode_f64(a, w.dtype)
+    return dict(q_nope=f(w.q_nope[ids]), q_pe=f(w.q_pe[ids]), w_uk=f(w.w_uk), w_uv=f(w.w_uv),
+                new_kv_c=f(w.new_kv_c[ids]), new_k_pe=f(w.new_k_pe[ids]), slots=slots,
+                storage=storage, offset=0, page=page, strides=(page * E, E, 1), block_table=table,
+                seq_lens=lens, scale=w.scale), lens
+
+
+def _blas_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_oracle_leg(w, budget_s: float = 12.0) -> dict:
+    """Time the float64 oracle's decode step on a bounded sample of the workload."""
+    from oracle import mla_oracle as orc
+    g = w.geom
+    n_total, t_total, bytes_total = 0, 0.0, 0
+    start = 0
+    while t_total < budget_s and n_total < w.batch:
+        n = 2
+        args, lens = oracle_sample(w, n, start)
+        t0 = time.perf_counter()
+        orc.decode_step(**args)
+        t_total += time.perf_counter() - t0
+        bytes_total += decode_algorithmic_bytes(lens, n, g.n_head, g.kv_rank, g.d_rope, 0)
+        n_total += n
+        start += n
+    return {"value": bytes_total / t_total / 1e9, "unit": UNIT, "cores": _blas_threads(),
+            "kind": "oracle",
+            "queries_per_s": n_total / t_total,
+            "sample": f"{n_total} of {w.batch} sequences of the same workload (their own blocks), "
+                      f"one decode step each, float64 numpy oracle; {t_total:.1f} s"}
+
+
+# --------------------------------------------------------------------------- the arms
+
+def run_reference(args) -> None:
+    """The oracle on the host cores, each step a bounded sample (one sequence, rotating)."""
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return
+    import mla_inputs as mi
+    from oracle import mla_oracle as orc
+    w = mi.v3_decode_large(materialize_cache=False)
+    g = w.geom
+    for i in range(args.warmup):
+        a, _ = oracle_sample(w, 1, i)
+        orc.decode_step(**a)
+    t_total, bytes_total, n = 0.0, 0, 0
+    for i in range(args.steps):
+        a, lens = oracle_sample(w, 1, args.warmup + i)
+        t0 = time.perf_counter()
+        orc.decode_step(**a)
+        t_total += time.perf_counter() - t0
+        bytes_total += decode_algorithmic_bytes(lens, 1, g.n_head, g.kv_rank, g.d_rope, 0)
+        n += 1
+    value = bytes_total / t_total / 1e9
+    cores = _blas_threads()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / max(n, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "queries_per_s": n / t_total,
+        "config": {"workload": WORKLOAD, "batch": w.batch, "heads": g.n_head, "page": w.page,
+                   "sample_per_step": "one sequence of the batch (rotating), its own blocks"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} sequences, one per step, float64 numpy oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args) -> None:
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = _dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+
+    import mla_latent_kv_11_gb300 as mla
+    from mla_latent_kv_11_gb300 import build as mla_build
+    import mla_inputs as mi
+    if rank == 0:
+        mla_build.build()
+    barrier()
+    mla.lib()
+
+    # Every rank runs its own batch of 64 sequences: weak scaling, no data-path collective.
+    w = mi.v3_decode_large(materialize_cache=True)
+    g = w.geom
+    step = DecodeStep(mla, w, device)
+    stream = torch.cuda.current_stream()
+    B, H, L, R = step.B, step.H, step.L, step.R
+    bytes_step = decode_algorithmic_bytes(w.seq_lens, B, H, L, R, 0)
+    flops_step = decode_algorithmic_flops(w.seq_lens, H, L, R)
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(_smi_id(local)) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        clk.mark_start()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step.run(ev_decode=evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        clk.mark_end()
+        barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total)
+    ms_step = ms_total / args.steps
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    clocks = clk.summary()
+
+    # end to end through the same calls with host buffers: pinned H2D of the step's inputs,
+    # the five calls, D2H of the output
+    def pinned(t):
+        return t.detach().cpu().pin_memory()
+
+    host = {k: pinned(getattr(step, k)) for k in ("q_nope", "q_pe", "new_kv_c", "new_k_pe", "slots",
+                                                    "table", "lens")}
+    dev_in = {k: torch.empty_like(getattr(step, k)) for k in host}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        step.run(**{"q_nope": dev_in["q_nope"], "q_pe": dev_in["q_pe"], "kv_c": dev_in["new_kv_c"],
+                    "k_pe": dev_in["new_k_pe"], "slots": dev_in["slots"], "table": dev_in["table"],
+                    "lens": dev_in["lens"]})
+        out_host.copy_(step.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+    barrier()
+
+    # component figures on their own workloads (not part of the step's value)
+    components = component_figures(mla, mi, device) if rank == 0 and not args.no_components else {}
+
+    cpu = cpu_oracle_leg(w) if rank == 0 and world == 1 and not args.no_cpu else None
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    total_bytes = bytes_step * world
+    value = total_bytes / (ms_step * 1e-3) / 1e9
+    achieved = bytes_step / (decode_ms * 1e-3) / 1e9
+    t_hbm = bytes_step / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops_step / (peaks["bf16_tflops"] * 1e12)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "queries_per_s": B * world / (ms_step * 1e-3),
+        "config": {"workload": WORKLOAD, "batch_per_gpu": B, "heads": H, "kv_lora_rank": L,
+                   "rope_dim": R, "page": w.page, "context": "U[1024,16384] per sequence",
+                   "cached_rows": int(w.seq_lens.sum()), "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "roofline": {"kernel": "mla_decode (schedule + split + combine)", "bound":
+                     "hbm" if t_hbm >= t_tc else "tensor", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": _traffic_for("attn_tc.cu") if os.path.exists(
+                         os.path.join(ROOT, "mla_latent_kv_11_gb300", "csrc", "attn_tc.cu")) else None,
+                     "peak_source": peaks["source"], "ms_per_launch": decode_ms,
+                     "bytes_per_launch": bytes_step, "flops_per_launch": flops_step,
+                     "tensor_frac": flops_step / (decode_ms * 1e-3) / (peaks["bf16_tflops"] * 1e12)},
+        "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "components": components,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def component_figures(mla, mi, device) -> dict:
+    """Per-stage figures on the other workloads: prefill TFLOP/s, concat and cache-write GB/s."""
+    import numpy as np
+    import torch
+    out = {}
+    peaks = _peaks()
+    torch.manual_seed(1234)
+
+    def timed(fn, reps=10, warm=3):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def dev(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(device).view(torch.bfloat16)
+
+    # NoPE causal prefill, 64 heads, 4 x 2048
+    H, L, page, n_seq, S = 64, 512, 64, 4, 2048
+    T = n_seq * S
+    q = torch.randn((T, H, L), device=device, dtype=torch.bfloat16) * 0.7
+    nb = T // page
+    cache = torch.randn((nb, page, L), device=device, dtype=torch.bfloat16)
+    table = torch.from_numpy(mi.permutation(4077, nb).astype(np.int32).reshape(n_seq, S // page)).to(device)
+    cu = torch.arange(0, T + 1, S, dtype=torch.int32, device=device)
+    kv = torch.full((n_seq,), S, dtype=torch.int32, device=device)
+    o = torch.empty((T, H, L), dtype=torch.bfloat16, device=device)
+    ms = timed(lambda: mla.mla_prefill(o, q, cache, table, cu, kv, S, L, 0, 1.0 / 16.0), reps=3, warm=1)
+    flops = n_seq * (S * (S + 1) // 2) * H * 2 * (L + L)
+    out["prefill_nope_h64_4x2048"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                                      "frac_of_bf16_peak": flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12)}
+    del q, cache, o
+    # concat and cache write, unified-slot workload
+    w = mi.write_concat_workload()
+    Nh, Bq, Lq = w.q_nope_storage.shape
+    store = dev(w.q_nope_storage)
+    nope = store.as_strided((Bq, Nh, Lq), (Lq, Bq * Lq, 1))
+    rope = dev(w.q_pe)
+    qc = torch.empty((Bq, Nh, Lq + w.q_pe.shape[2]), dtype=torch.bfloat16, device=device)
+    ms = timed(lambda: mla.mla_concat_q(qc, nope, rope), reps=50)
+    nbytes = 2 * qc.numel() * 2
+    out["concat_q_64x128"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    E = w.entry
+    big = torch.zeros((w.num_blocks, w.n_layers * w.page * E), dtype=torch.bfloat16, device=device)
+    view = big.view(-1).as_strided((w.num_blocks, w.page, E), (w.n_layers * w.page * E, E, 1),
+                                   w.layer * w.page * E)
+    kv_c, k_pe = dev(w.kv_c), dev(w.k_pe)
+    slots = torch.from_numpy(w.slots).to(device)
+    ms = timed(lambda: mla.mla_cache_write(view, kv_c, k_pe, slots), reps=50)
+    nbytes = 2 * w.kv_c.shape[0] * E * 2 + w.slots.size * 8
+    out["cache_write_200tok_unified_view"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    return out
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-components", action="store_true", help="skip the per-stage figures")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

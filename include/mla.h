@@ -1,0 +1,192 @@
+/*
+ * mla.h - C ABI of the weight-absorbed Multi-head Latent Attention (MLA) hot
+ * path over a paged latent KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * One decode step is five calls, all asynchronous on the caller's stream:
+ *
+ *   mla_absorb_q    q_lat[h,b,:] = q_nope[h,b,:] @ W_UK[h]        (step 1)
+ *   mla_concat_q    q_cat[t,h,:] = [q_lat[t,h,:] | q_pe[t,h,:]]    (step 2)
+ *   mla_cache_write cache[slot]  = [kv_c | k_pe]                   (step 3)
+ *   mla_decode      o_lat = softmax(scale * q_cat . cache) c_kv    (step 4)
+ *   mla_v_up        out[h,b,:]   = o_lat[h,b,:] @ W_UV[h]          (step 5)
+ *
+ * and mla_prefill is step 4 for many causal queries per sequence.
+ *
+ * Sources of the operations (web pages):
+ *   [vt]    vllm.cpp, tests/vt/test_ops_mla_absorb.cpp (BatchedMatmul and
+ *           ConcatMlaNopeRope test cases; strided views Contig/View3).
+ *   [memra] memra-engine 0.124.1, tests/mla_gpu_forward.rs (absorbed and naive
+ *           oracles; cache rows [c_kv | k_pe]; causal prefill and stepwise decode).
+ *   [vllm]  vLLM, tests/kernels/attention/test_mla_cross_layer_kernel_equivalence.py
+ *           (concat_and_cache_mla into a unified-slot layer view; paged dense
+ *           decode with a block table and cache_seqlens).
+ *
+ * Conventions shared by every call
+ *   - Ownership: the caller allocates and owns every buffer. Unless a call says
+ *     otherwise the library allocates no device memory; it keeps a host-side
+ *     cache of TMA tensor maps and a few bytes of static device state (an
+ *     error word per kernel module).
+ *   - Pointers: every data pointer is a DEVICE pointer of the current CUDA
+ *     device. `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Execution: asynchronous; no call synchronises the stream or the device.
+ *   - Views: an mla_tensor is {data, rank, shape, stride}; strides count
+ *     ELEMENTS and `data` already includes any storage offset ([vt] View3).
+ *     The innermost stride must be 1 on every tensor ([vt] "rejects malformed
+ *     shapes/strides rather than mis-computing").
+ *   - Validation: shapes, strides, dtypes, null pointers and alignment are
+ *     checked on the host before any launch. A failed check returns
+ *     MLA_ERR_INVALID_ARG (malformed) or MLA_ERR_UNSUPPORTED (well formed but
+ *     outside what the kernels handle) and launches nothing.
+ *   - Device-resident values (slots, block ids, sequence lengths) cannot be
+ *     checked on the host. The kernels check them: an access that would leave
+ *     the cache view is skipped and recorded; mla_device_error() reports it.
+ *   - Empty work (zero tokens, zero sequences) returns MLA_OK and launches
+ *     nothing ([memra]: "never a zero-extent launch").
+ *   - Errors: mla_last_error() returns a message for the calling thread's
+ *     last failed call. Launch failures return MLA_ERR_CUDA.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_ABI_VERSION 1
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,  /* malformed shape, stride, dtype or pointer   */
+  MLA_ERR_UNSUPPORTED = 2,  /* well formed, but not handled by the kernels  */
+  MLA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed         */
+  MLA_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up           */
+  MLA_ERR_DEVICE_DATA = 5   /* a device-resident index was out of range     */
+} mla_status;
+
+typedef enum {
+  MLA_F32 = 0,   /* IEEE binary32 */
+  MLA_BF16 = 1   /* bfloat16; results rounded to nearest even */
+} mla_dtype;
+
+/* A strided view: element (i0,..,i_{rank-1}) lives at
+ * data + sum_k i_k * stride[k] elements. rank <= 4; unused entries ignored. */
+typedef struct {
+  void* data;
+  int32_t rank;
+  int64_t shape[4];
+  int64_t stride[4];
+} mla_tensor;
+
+/* ABI version of the loaded library (MLA_ABI_VERSION at build time). */
+int mla_abi_version(void);
+
+/* Message for the calling thread's last failed call ("" if none). The string
+ * stays valid until the thread's next call into the library. */
+const char* mla_last_error(void);
+
+/* Static name of a status code. */
+const char* mla_status_string(mla_status status);
+
+/* Step 1 - W_UK absorption ([vt] BatchedMatmul, q-side fold: a (B,N,P) -> (N,B,P)
+ * transposed view times W_UK_T [N,P,L]; [memra] mla_absorb_q).
+ *   q_lat_out [H,B,L] (written), q_nope [H,B,P], w_uk [H,P,L]; any strides with
+ *   innermost 1 (q_nope is usually the transpose of a [B,H,P] buffer and
+ *   q_lat_out the transpose of a [B,H,L] buffer).
+ *   q_lat[h,b,l] = sum_p q_nope[h,b,p] * w_uk[h,p,l], accumulated in fp32 and
+ *   stored in `dtype`. All three tensors have `dtype`. */
+mla_status mla_absorb_q(mla_dtype dtype, mla_tensor q_lat_out, mla_tensor q_nope,
+                        mla_tensor w_uk, void* stream);
+
+/* Step 2 - q concat ([vt] ConcatMlaNopeRope: a pure copy, bit for bit, that must
+ * follow the strides of a transposed nope operand; a rope operand with one head
+ * is broadcast to every head, as for _concat_k_nope_k_pe).
+ *   q_cat_out [T,H,L+R] (written), nope [T,H,L], rope [T,H,R] or [T,1,R]
+ *   (a rope stride(1) of 0 also broadcasts). Bits are copied unchanged,
+ *   including NaN payloads and signed zeros. R may be 0. */
+mla_status mla_concat_q(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope,
+                        mla_tensor rope, void* stream);
+
+/* Step 3 - paged latent cache write ([vllm] concat_and_cache_mla with kv_cache_dtype
+ * "auto"; [memra] mla_append_latent).
+ *   cache [num_blocks, page, L+R] view (written): any stride(0) and storage
+ *   offset, e.g. one layer of a block-major unified slot; kv_c [T,L], k_pe [T,R];
+ *   slot_mapping: device int64 [num_tokens].
+ *   For token i with s = slot_mapping[i] >= 0:
+ *     cache[s / page, s % page, 0:L]   = kv_c[i]
+ *     cache[s / page, s % page, L:L+R] = k_pe[i]
+ *   bit for bit. Negative slots are padding and write nothing. Slots at or beyond
+ *   num_blocks*page write nothing and set MLA_ERR_DEVICE_DATA in mla_device_error.
+ *   No element outside the addressed rows is written. Duplicate slots: the
+ *   surviving row is unspecified. */
+mla_status mla_cache_write(mla_dtype dtype, mla_tensor cache, mla_tensor kv_c, mla_tensor k_pe,
+                           const int64_t* slot_mapping, int64_t num_tokens, void* stream);
+
+/* Step 4 - paged split-KV decode ([vllm] flash_mla_with_kvcache / FlashInfer MLA
+ * decode over a strided cache view; [memra] mla_attn_absorbed with t_q = 1).
+ *   o_lat_out [B,H,L] (written; `dtype`), lse_out: device float [B,H] contiguous
+ *   or NULL; q_cat [B,H,L+R]; cache as in mla_cache_write;
+ *   block_table: device int32 [B, max_blocks] with row stride block_table_stride;
+ *   seq_lens: device int32 [B].
+ *   For every sequence b and head h, over rows t < seq_lens[b] of the cache
+ *   (row t at block block_table[b, t / page], offset t % page):
+ *     s_t = softmax_scale * (q_cat[b,h,0:L] . c_kv_t + q_cat[b,h,L:] . k_pe_t)
+ *     o_lat[b,h,:] = sum_t softmax(s)_t * c_kv_t,  lse[b,h] = ln sum_t e^{s_t}
+ *   with fp32 softmax and accumulation. seq_lens[b] == 0 gives o = 0 and
+ *   lse = -inf. The context is cut into chunks processed in parallel and merged
+ *   by their LSE; num_splits > 0 sets the number of chunks processed in
+ *   parallel over the whole batch (0 = chosen from the SM count). For fixed
+ *   (seq_lens, num_splits, device) the result is bit-identical from run to run
+ *   and does not depend on the cache strides.
+ *   workspace: device scratch of at least mla_decode_workspace_size(...) bytes,
+ *   256-byte aligned, owned by the caller, not used by concurrent calls. */
+mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                      mla_tensor cache, const int32_t* block_table, int64_t block_table_stride,
+                      int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank,
+                      int32_t rope_dim, float softmax_scale, int32_t num_splits,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace mla_decode needs for `batch` sequences of `num_heads` heads
+ * with latent width `kv_lora_rank` and the given num_splits (0 = automatic) on
+ * the current device. */
+size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank,
+                                 int32_t num_splits);
+
+/* Step 4, prefill - causal attention of many queries per sequence over the same
+ * paged cache ([memra] gate 1: pure prefill t_q == t_kv and the chunked shape
+ * where the queries are a suffix of an already populated cache).
+ *   o_lat_out [T,H,L] (written), lse_out device float [T,H] or NULL,
+ *   q_cat [T,H,L+R] with the queries of sequence b in rows
+ *   cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 (device int32 [batch+1]);
+ *   seq_lens_kv: device int32 [batch], rows of sequence b already in the cache
+ *   (including its own queries' rows).
+ *   Query i of sequence b sits at position p = seq_lens_kv[b] - q_len_b + i and
+ *   attends rows 0..p (bottom-right causal alignment); otherwise as mla_decode.
+ *   max_q_len bounds q_len_b. No workspace is needed: pass NULL and 0. */
+mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                       mla_tensor cache, const int32_t* block_table, int64_t block_table_stride,
+                       int32_t max_blocks, const int32_t* cu_seqlens_q, const int32_t* seq_lens_kv,
+                       int32_t batch, int32_t max_q_len, int32_t kv_lora_rank, int32_t rope_dim,
+                       float softmax_scale, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Step 5 - W_UV un-projection ([vt] BatchedMatmul at the _v_up_proj call site: a
+ * (B,N,L) -> (N,B,L) transposed input, output written into a transposed (B,N,V);
+ * [memra] mla_decompress_v).
+ *   out [H,B,V] (written), o_lat [H,B,L], w_uv [H,L,V].
+ *   out[h,b,v] = sum_l o_lat[h,b,l] * w_uv[h,l,v], fp32 accumulation. */
+mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tensor w_uv,
+                    void* stream);
+
+/* Synchronises `stream`, then reports and clears the device-side error words the
+ * kernels set (out-of-range slot, block id or length: MLA_ERR_DEVICE_DATA; a
+ * bounded wait that gave up: MLA_ERR_TIMEOUT). MLA_OK if none was set. */
+mla_status mla_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

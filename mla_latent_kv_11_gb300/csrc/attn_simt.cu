@@ -1,0 +1,466 @@
+// Step 4 on CUDA cores: the split-KV schedule, the LSE combine, and the general
+// (any head count, any dtype) decode and prefill kernels.
+//
+// Schedule. The batch's context is cut into tiles of kTile rows; sequence b
+// owns ceil(len_b / kTile) tiles and tile_prefix is their prefix sum. With
+// W = min(units, total) work units, unit w takes the contiguous global range
+//   [floor(w*total/W), floor((w+1)*total/W)),
+// so every unit gets the same number of tiles (at least one) whatever the
+// length mix; units past W have nothing to do. A unit
+// that covers a whole sequence writes the final output; a sequence cut across
+// n > 1 units gets n partial slots (normalised o and LSE), merged afterwards by
+// the combine kernel. The schedule depends only on the lengths and W: results
+// are run-to-run bit-identical and do not depend on the cache strides.
+//
+// SIMT attention. One CTA holds the queries of a group of up to 16 heads of one
+// token in shared memory (fp32), streams the key rows of its range in tiles of
+// 32 (through the block table), computes the 16 x 32 scores, runs the online
+// softmax per head with warp shuffles and accumulates o_lat (each thread owns
+// 2 latent columns of every head of the group).
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+__device__ unsigned g_attn_err = 0;
+
+constexpr int kHeads = 16;    // heads per CTA
+constexpr int kKeys = 32;     // keys per inner tile
+constexpr int kThreads = 256;
+constexpr int kMaxL = 512;    // latent columns per thread pair: 2 * 256
+
+__device__ __forceinline__ float ld(const float* p) { return *p; }
+__device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tot[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
+  *total = warp_tot[31];
+  __syncthreads();
+  return before;
+}
+
+__device__ __forceinline__ int clamp_len(const int32_t* seq_lens, int b, int cap) {
+  int n = seq_lens[b];
+  if (n < 0 || n > cap) {
+    atomicOr(&g_attn_err, kErrDeviceData);
+    n = n < 0 ? 0 : cap;
+  }
+  return n;
+}
+
+__device__ __forceinline__ int unit_begin(int w, int total, int W) {
+  return (int)(((long long)w * total) / W);
+}
+// The unit whose range holds global tile t (the last unit with begin <= t).
+__device__ __forceinline__ int unit_of(int t, int total, int W) {
+  return (int)((((long long)t + 1) * W - 1) / total);
+}
+
+__global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __restrict__ seq_lens,
+                                                               int B, int cap, DecodeSched s) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry_sh;
+  if (threadIdx.x == 0) carry_sh = 0;
+  __syncthreads();
+  // pass 1: tile prefix
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + threadIdx.x;
+    const int n = b < B ? (clamp_len(seq_lens, b, cap) + kTile - 1) / kTile : 0;
+    int tot;
+    const int ex = block_exclusive_scan(n, warp_tot, &tot);
+    const int carry = carry_sh;
+    if (b < B) s.tile_prefix[b] = carry + ex;
+    __syncthreads();
+    if (threadIdx.x == 0) carry_sh = carry + tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) s.tile_prefix[B] = carry_sh;
+  __syncthreads();
+  const int total = carry_sh;
+  const int W = min(s.units, total);  // every unit in use gets at least one tile
+  __syncthreads();
+  if (threadIdx.x == 0) carry_sh = 0;
+  __syncthreads();
+  // pass 2: units touching each sequence, and partial-slot bases
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + threadIdx.x;
+    int np = 0, fu = 0;
+    if (b < B) {
+      const int t0 = s.tile_prefix[b], t1 = s.tile_prefix[b + 1];
+      if (t1 > t0) {
+        fu = unit_of(t0, total, W);
+        np = unit_of(t1 - 1, total, W) - fu + 1;
+      }
+      s.first_unit[b] = fu;
+      s.npieces[b] = np;
+    }
+    int tot;
+    const int ex = block_exclusive_scan(np > 1 ? np : 0, warp_tot, &tot);
+    const int carry = carry_sh;
+    if (b < B) s.piece_base[b] = carry + ex;
+    __syncthreads();
+    if (threadIdx.x == 0) carry_sh = carry + tot;
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Attention of one query token (heads [h0, h0+hn)) over cache rows [k0, k1).
+// Returns per thread the unnormalised accumulators, and in shared memory the
+// running max m_sh and denominator l_sh of each head.
+// Shared memory of the SIMT attention: q [kHeads][E+1] and k [kKeys][E+1] fp32
+// (odd pitch: a warp reading one column of 32 rows hits 32 banks), then the
+// probabilities and the per-head softmax state.
+struct SimtSmem {
+  float* q;
+  float* k;
+  float (*p)[kKeys];
+  float* m;
+  float* l;
+  float* alpha;
+  int pitch;
+};
+
+__host__ __device__ inline size_t simt_smem_bytes(int E) {
+  const int pitch = E + 1;
+  return sizeof(float) * ((size_t)(kHeads + kKeys) * pitch + kHeads * kKeys + 3 * kHeads);
+}
+
+__device__ inline SimtSmem simt_smem(unsigned char* raw, int E) {
+  SimtSmem s;
+  s.pitch = E + 1;
+  float* f = reinterpret_cast<float*>(raw);
+  s.q = f;
+  s.k = s.q + kHeads * s.pitch;
+  s.p = reinterpret_cast<float(*)[kKeys]>(s.k + kKeys * s.pitch);
+  s.m = reinterpret_cast<float*>(s.p + kHeads);
+  s.l = s.m + kHeads;
+  s.alpha = s.l + kHeads;
+  return s;
+}
+
+template <typename T>
+__device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int64_t q_s_head,
+                            int h0, int hn, int E, int L, const CacheView& cv,
+                            const int32_t* __restrict__ bt_row, int k0, int k1, float scale,
+                            float (&acc)[kHeads][2]) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = sm.pitch;
+  __syncthreads();  // the previous segment's epilogue may still read m and l
+  for (int i = tid; i < kHeads * E; i += kThreads) {
+    const int h = i / E, e = i - h * E;
+    sm.q[h * P + e] = h < hn ? ld(q_row + (int64_t)(h0 + h) * q_s_head + e) : 0.f;
+  }
+  if (tid < kHeads) {
+    sm.m[tid] = -CUDART_INF_F;
+    sm.l[tid] = 0.f;
+  }
+#pragma unroll
+  for (int h = 0; h < kHeads; ++h) acc[h][0] = acc[h][1] = 0.f;
+  const T* cache = static_cast<const T*>(cv.data);
+  for (int kt = k0; kt < k1; kt += kKeys) {
+    __syncthreads();
+    // stage key rows kt .. kt+31 (rows past k1 are zero and masked below)
+    for (int i = tid; i < kKeys * E; i += kThreads) {
+      const int j = i / E, e = i - j * E;
+      const int t = kt + j;
+      float v = 0.f;
+      if (t < k1) {
+        const int blk = bt_row[t / cv.page];
+        if (blk >= 0 && blk < cv.num_blocks)
+          v = ld(cache + (int64_t)blk * cv.s_blk + (int64_t)(t % cv.page) * cv.s_row + e);
+        else if (e == 0)
+          atomicOr(&g_attn_err, kErrDeviceData);
+      }
+      sm.k[j * P + e] = v;
+    }
+    __syncthreads();
+    // scores: warp w owns heads 2w, 2w+1; lane owns key kt + lane
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = 2 * warp + hh;
+      float s = 0.f;
+      for (int e = 0; e < E; ++e) s = fmaf(sm.q[h * P + e], sm.k[lane * P + e], s);
+      s = (kt + lane < k1) ? s * scale : -CUDART_INF_F;
+      float mx = s;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_old = sm.m[h];
+      const float m_new = fmaxf(m_old, mx);
+      const float p = (s == -CUDART_INF_F) ? 0.f : __expf(s - m_new);
+      float sum = p;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      sm.p[h][lane] = p;
+      __syncwarp();
+      if (lane == 0) {
+        const float a = (m_old == -CUDART_INF_F) ? 0.f : __expf(m_old - m_new);
+        sm.alpha[h] = a;
+        sm.l[h] = sm.l[h] * a + sum;
+        sm.m[h] = m_new;
+      }
+    }
+    __syncthreads();
+    // o_lat accumulators: thread owns latent columns tid and tid + 256 of every head
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int l = tid + c * kThreads;
+      if (l < L) {
+        float kv[kKeys];
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) kv[j] = sm.k[j * P + l];
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) {
+          float a = acc[h][c] * sm.alpha[h];
+#pragma unroll
+          for (int j = 0; j < kKeys; ++j) a = fmaf(sm.p[h][j], kv[j], a);
+          acc[h][c] = a;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
+    T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
+    const T* __restrict__ q, int64_t q_s0, int64_t q_s1, CacheView cv,
+    const int32_t* __restrict__ block_table, int64_t bt_stride,
+    const int32_t* __restrict__ seq_lens, int cap, int B, int H, int L, int R, float scale,
+    DecodeSched s) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const SimtSmem sm = simt_smem(smem_raw, L + R);
+  const int total = s.tile_prefix[B];
+  const int W = min(s.units, total), w = blockIdx.x;
+  if (w >= W) return;
+  const int h0 = blockIdx.y * kHeads, hn = min(kHeads, H - h0);
+  const int t0 = unit_begin(w, total, W), t1 = unit_begin(w + 1, total, W);
+  const int E = L + R;
+  // first sequence: the last b with tile_prefix[b] <= t0
+  int lo = 0, hi = B;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s.tile_prefix[mid] <= t0) lo = mid; else hi = mid - 1;
+  }
+  int b = lo;
+  float acc[kHeads][2];
+  for (int t = t0; t < t1;) {
+    while (s.tile_prefix[b + 1] <= t) ++b;
+    const int seg_end = min(t1, s.tile_prefix[b + 1]);
+    const int len = min(max(seq_lens[b], 0), cap);
+    const int k0 = (t - s.tile_prefix[b]) * kTile;
+    const int k1 = min((seg_end - s.tile_prefix[b]) * kTile, len);
+    attend_rows<T>(sm, q + (int64_t)b * q_s0, q_s1, h0, hn, E, L, cv,
+                   block_table + (int64_t)b * bt_stride, k0, k1, scale, acc);
+    const bool whole = s.npieces[b] == 1;
+    const int slot = whole ? 0 : s.piece_base[b] + (w - s.first_unit[b]);
+    for (int h = 0; h < hn; ++h) {
+      const float l = sm.l[h];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse = l > 0.f ? sm.m[h] + logf(l) : -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col = threadIdx.x + c * kThreads;
+        if (col < L) {
+          const float v = acc[h][c] * inv;
+          if (whole)
+            st(o_lat + (int64_t)b * o_s0 + (int64_t)(h0 + h) * o_s1 + col, v);
+          else
+            s.part_o[((int64_t)slot * H + h0 + h) * L + col] = v;
+        }
+      }
+      if (threadIdx.x == 0) {
+        if (whole) {
+          if (lse_out) lse_out[(int64_t)b * H + h0 + h] = lse;
+        } else {
+          s.part_lse[(int64_t)slot * H + h0 + h] = lse;
+        }
+      }
+    }
+    t = seg_end;
+  }
+}
+
+// Merge the partials of every sequence cut across several units; write o = 0
+// and lse = -inf for empty sequences. One CTA per (sequence, head).
+template <typename T>
+__global__ void __launch_bounds__(128) decode_combine_kernel(
+    T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
+    int B, int H, int L, DecodeSched s) {
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int np = s.npieces[b];
+  if (np == 1) return;
+  T* o = o_lat + (int64_t)b * o_s0 + (int64_t)h * o_s1;
+  if (np == 0) {
+    for (int c = threadIdx.x; c < L; c += blockDim.x) st(o + c, 0.f);
+    if (threadIdx.x == 0 && lse_out) lse_out[(int64_t)b * H + h] = -CUDART_INF_F;
+    return;
+  }
+  const int base = s.piece_base[b];
+  float m = -CUDART_INF_F;
+  for (int i = 0; i < np; ++i) m = fmaxf(m, s.part_lse[(int64_t)(base + i) * H + h]);
+  float tot = 0.f;
+  for (int i = 0; i < np; ++i) {
+    const float li = s.part_lse[(int64_t)(base + i) * H + h];
+    tot += li == -CUDART_INF_F ? 0.f : __expf(li - m);
+  }
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  for (int c = threadIdx.x; c < L; c += blockDim.x) {
+    float v = 0.f;
+    for (int i = 0; i < np; ++i) {
+      const float li = s.part_lse[(int64_t)(base + i) * H + h];
+      const float wgt = li == -CUDART_INF_F ? 0.f : __expf(li - m);
+      v = fmaf(wgt, s.part_o[((int64_t)(base + i) * H + h) * L + c], v);
+    }
+    st(o + c, v * inv);
+  }
+  if (threadIdx.x == 0 && lse_out)
+    lse_out[(int64_t)b * H + h] = tot > 0.f ? m + logf(tot) : -CUDART_INF_F;
+}
+
+// Causal prefill: one CTA per (query row, head group), no split.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) prefill_simt_kernel(
+    T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
+    const T* __restrict__ q, int64_t q_s0, int64_t q_s1, CacheView cv,
+    const int32_t* __restrict__ block_table, int64_t bt_stride, int max_blocks,
+    const int32_t* __restrict__ cu_q, const int32_t* __restrict__ kv_lens, int B, int H, int L,
+    int R, float scale) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const SimtSmem sm = simt_smem(smem_raw, L + R);
+  const int r = blockIdx.x;
+  const int h0 = blockIdx.y * kHeads, hn = min(kHeads, H - h0);
+  // the sequence holding global query row r: last b with cu_q[b] <= r
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_q[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int q_len = cu_q[b + 1] - cu_q[b];
+  const int i = r - cu_q[b];
+  const int kv = clamp_len(kv_lens, b, max_blocks * cv.page);
+  int end = 0;
+  if (i >= 0 && i < q_len) end = min(kv, max(0, kv - q_len + i + 1));
+  float acc[kHeads][2];
+  attend_rows<T>(sm, q + (int64_t)r * q_s0, q_s1, h0, hn, L + R, L, cv,
+                 block_table + (int64_t)b * bt_stride, 0, end, scale, acc);
+  for (int h = 0; h < hn; ++h) {
+    const float l = sm.l[h];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int col = threadIdx.x + c * kThreads;
+      if (col < L) st(o_lat + (int64_t)r * o_s0 + (int64_t)(h0 + h) * o_s1 + col, acc[h][c] * inv);
+    }
+    if (threadIdx.x == 0 && lse_out)
+      lse_out[(int64_t)r * H + h0 + h] = l > 0.f ? sm.m[h] + logf(l) : -CUDART_INF_F;
+  }
+}
+
+template <typename K>
+void allow_smem(K k, size_t bytes) {
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
+                                   int32_t page, const DecodeSched& s, cudaStream_t st) {
+  const long long cap = (long long)max_blocks * page;
+  decode_schedule_kernel<<<1, 1024, 0, st>>>(seq_lens, B, (int)(cap > INT32_MAX ? INT32_MAX : cap), s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
+                               const CacheView& cache, const int32_t* block_table,
+                               int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t H,
+                               int32_t L, int32_t R, float scale, const DecodeSched& s,
+                               cudaStream_t st) {
+  const dim3 grid(s.units, (H + kHeads - 1) / kHeads);
+  const long long cap_ll = (long long)max_blocks * cache.page;
+  const int cap = (int)(cap_ll > INT32_MAX ? INT32_MAX : cap_ll);
+  const size_t sm = simt_smem_bytes(L + R);
+  if (dt == MLA_F32) {
+    allow_smem(decode_split_simt_kernel<float>, sm);
+    decode_split_simt_kernel<float><<<grid, kThreads, sm, st>>>(
+        (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
+        block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s);
+  } else {
+    allow_smem(decode_split_simt_kernel<__nv_bfloat16>, sm);
+    decode_split_simt_kernel<__nv_bfloat16><<<grid, kThreads, sm, st>>>(
+        (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
+        q.s1, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_combine(mla_dtype dt, const View3& o_lat, float* lse,
+                                  const int32_t* seq_lens, int32_t B, int32_t H, int32_t L,
+                                  const DecodeSched& s, cudaStream_t st) {
+  (void)seq_lens;
+  const dim3 grid(B, H);
+  if (dt == MLA_F32)
+    decode_combine_kernel<float><<<grid, 128, 0, st>>>((float*)o_lat.data, o_lat.s0, o_lat.s1, lse,
+                                                       B, H, L, s);
+  else
+    decode_combine_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(
+        (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, B, H, L, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
+                                const CacheView& cache, const int32_t* block_table,
+                                int64_t bt_stride, int32_t max_blocks, const int32_t* cu_q,
+                                const int32_t* kv_lens, int32_t B, int32_t T, int32_t H,
+                                int32_t L, int32_t R, float scale, cudaStream_t st) {
+  const dim3 grid(T, (H + kHeads - 1) / kHeads);
+  const size_t sm = simt_smem_bytes(L + R);
+  if (dt == MLA_F32) {
+    allow_smem(prefill_simt_kernel<float>, sm);
+    prefill_simt_kernel<float><<<grid, kThreads, sm, st>>>(
+        (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
+        block_table, bt_stride, max_blocks, cu_q, kv_lens, B, H, L, R, scale);
+  } else {
+    allow_smem(prefill_simt_kernel<__nv_bfloat16>, sm);
+    prefill_simt_kernel<__nv_bfloat16><<<grid, kThreads, sm, st>>>(
+        (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
+        q.s1, cache, block_table, bt_stride, max_blocks, cu_q, kv_lens, B, H, L, R, scale);
+  }
+  return cudaGetLastError();
+}
+
+unsigned attn_simt_errors_read_clear() {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_attn_err, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_attn_err, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace mla

@@ -1,0 +1,340 @@
+// Host side of the C ABI: argument validation, dispatch, error reporting.
+// Nothing in this file touches device memory except through the launchers.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+thread_local char g_msg[512] = "";
+
+mla_status fail(mla_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+mla_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MLA_OK;
+  return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int64_t numel(const mla_tensor& t) {
+  int64_t n = 1;
+  for (int i = 0; i < t.rank; ++i) n *= t.shape[i];
+  return n;
+}
+
+size_t esize(mla_dtype dt) { return dt == MLA_F32 ? 4 : 2; }
+
+// Well-formedness of one view: rank, non-negative sizes, non-null data when
+// non-empty, innermost stride 1 (the one layout rule the source tests assert).
+mla_status check_view(const mla_tensor& t, int rank, const char* name) {
+  if (t.rank != rank) return fail(MLA_ERR_INVALID_ARG, "%s: rank %d, expected %d", name, t.rank, rank);
+  for (int i = 0; i < rank; ++i)
+    if (t.shape[i] < 0) return fail(MLA_ERR_INVALID_ARG, "%s: negative shape[%d]", name, i);
+  if (numel(t) == 0) return MLA_OK;
+  if (t.data == nullptr) return fail(MLA_ERR_INVALID_ARG, "%s: null data", name);
+  if (t.stride[rank - 1] != 1)
+    return fail(MLA_ERR_INVALID_ARG, "%s: innermost stride %lld, must be 1", name,
+                (long long)t.stride[rank - 1]);
+  for (int i = 0; i < rank - 1; ++i)
+    if (t.stride[i] < 0) return fail(MLA_ERR_INVALID_ARG, "%s: negative stride[%d]", name, i);
+  return MLA_OK;
+}
+
+#define MLA_TRY(expr)                 \
+  do {                                \
+    mla_status s__ = (expr);          \
+    if (s__ != MLA_OK) return s__;    \
+  } while (0)
+
+mla_status check_dtype(mla_dtype dt) {
+  if (dt != MLA_F32 && dt != MLA_BF16) return fail(MLA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  return MLA_OK;
+}
+
+// Shared validation of the three bmm operands: out [G,M,N] = a [G,M,K] @ b [G,K,N].
+mla_status check_bmm(const mla_tensor& out, const mla_tensor& a, const mla_tensor& b,
+                     const char* on, const char* an, const char* bn) {
+  MLA_TRY(check_view(out, 3, on));
+  MLA_TRY(check_view(a, 3, an));
+  MLA_TRY(check_view(b, 3, bn));
+  if (a.shape[0] != b.shape[0] || out.shape[0] != a.shape[0])
+    return fail(MLA_ERR_INVALID_ARG, "batch (head) mismatch: %s %lld, %s %lld, %s %lld", an,
+                (long long)a.shape[0], bn, (long long)b.shape[0], on, (long long)out.shape[0]);
+  if (a.shape[2] != b.shape[1])
+    return fail(MLA_ERR_INVALID_ARG, "inner dimension mismatch: %s K=%lld, %s K=%lld", an,
+                (long long)a.shape[2], bn, (long long)b.shape[1]);
+  if (out.shape[1] != a.shape[1] || out.shape[2] != b.shape[2])
+    return fail(MLA_ERR_INVALID_ARG, "%s shape [%lld,%lld,%lld] does not match the product", on,
+                (long long)out.shape[0], (long long)out.shape[1], (long long)out.shape[2]);
+  if (a.shape[2] > 4096) return fail(MLA_ERR_UNSUPPORTED, "inner dimension %lld > 4096", (long long)a.shape[2]);
+  if (a.shape[0] > 65535 || a.shape[1] > 65535LL * 8 || b.shape[2] > INT32_MAX / 2)
+    return fail(MLA_ERR_UNSUPPORTED, "bmm shape beyond the launch limits");
+  return MLA_OK;
+}
+
+mla_status check_cache(const mla_tensor& cache, int64_t E, const char* name) {
+  MLA_TRY(check_view(cache, 3, name));
+  if (cache.shape[2] != E)
+    return fail(MLA_ERR_INVALID_ARG, "%s: entry width %lld, expected L+R = %lld", name,
+                (long long)cache.shape[2], (long long)E);
+  if (cache.shape[1] <= 0 || cache.shape[0] <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "%s: empty cache", name);
+  if (cache.shape[0] > INT32_MAX || cache.shape[1] > INT32_MAX)
+    return fail(MLA_ERR_UNSUPPORTED, "%s: too many blocks or rows per block", name);
+  return MLA_OK;
+}
+
+}  // namespace
+
+DecodeWsLayout decode_ws_layout(int64_t B, int64_t H, int64_t L, int64_t units) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  DecodeWsLayout l{};
+  size_t off = 0;
+  l.off_prefix = off; off = up(off + sizeof(int32_t) * (B + 1));
+  l.off_first = off;  off = up(off + sizeof(int32_t) * B);
+  l.off_np = off;     off = up(off + sizeof(int32_t) * B);
+  l.off_base = off;   off = up(off + sizeof(int32_t) * B);
+  const int64_t pieces = B + units;
+  l.off_part_o = off;   off = up(off + sizeof(float) * pieces * H * L);
+  l.off_part_lse = off; off = up(off + sizeof(float) * pieces * H);
+  l.total = off;
+  return l;
+}
+
+DecodeSched decode_sched_from_ws(void* ws, const DecodeWsLayout& lay, int32_t B, int32_t units) {
+  char* p = static_cast<char*>(ws);
+  DecodeSched s;
+  s.tile_prefix = reinterpret_cast<int32_t*>(p + lay.off_prefix);
+  s.first_unit = reinterpret_cast<int32_t*>(p + lay.off_first);
+  s.npieces = reinterpret_cast<int32_t*>(p + lay.off_np);
+  s.piece_base = reinterpret_cast<int32_t*>(p + lay.off_base);
+  s.part_o = reinterpret_cast<float*>(p + lay.off_part_o);
+  s.part_lse = reinterpret_cast<float*>(p + lay.off_part_lse);
+  s.units = units;
+  s.max_pieces = B + units;
+  return s;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> g(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Work units of the split-KV decode: explicit, or two per SM.
+static int32_t decode_units(int32_t num_splits) {
+  if (num_splits > 0) return num_splits;
+  return 2 * device_sm_count();
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char* mla_last_error(void) { return g_msg; }
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_DEVICE_DATA: return "MLA_ERR_DEVICE_DATA";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+mla_status mla_absorb_q(mla_dtype dtype, mla_tensor q_lat_out, mla_tensor q_nope, mla_tensor w_uk,
+                        void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_bmm(q_lat_out, q_nope, w_uk, "q_lat_out", "q_nope", "w_uk"));
+  if (numel(q_lat_out) == 0) return MLA_OK;
+  return cuda_status(launch_bmm_simt(dtype, view3(q_lat_out), view3(q_nope), view3(w_uk),
+                                     (cudaStream_t)stream), "mla_absorb_q");
+}
+
+mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tensor w_uv,
+                    void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_bmm(out, o_lat, w_uv, "out", "o_lat", "w_uv"));
+  if (numel(out) == 0) return MLA_OK;
+  return cuda_status(launch_bmm_simt(dtype, view3(out), view3(o_lat), view3(w_uv),
+                                     (cudaStream_t)stream), "mla_v_up");
+}
+
+mla_status mla_concat_q(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope, mla_tensor rope,
+                        void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat_out, 3, "q_cat_out"));
+  MLA_TRY(check_view(nope, 3, "nope"));
+  MLA_TRY(check_view(rope, 3, "rope"));
+  const int64_t T = q_cat_out.shape[0], H = q_cat_out.shape[1];
+  if (nope.shape[0] != T || nope.shape[1] != H)
+    return fail(MLA_ERR_INVALID_ARG, "nope [%lld,%lld,.] does not match q_cat_out [%lld,%lld,.]",
+                (long long)nope.shape[0], (long long)nope.shape[1], (long long)T, (long long)H);
+  if (rope.shape[0] != T || (rope.shape[1] != H && rope.shape[1] != 1))
+    return fail(MLA_ERR_INVALID_ARG, "rope must be [T,H,R] or [T,1,R]");
+  if (nope.shape[2] + rope.shape[2] != q_cat_out.shape[2])
+    return fail(MLA_ERR_INVALID_ARG, "q_cat_out width %lld != L + R = %lld",
+                (long long)q_cat_out.shape[2], (long long)(nope.shape[2] + rope.shape[2]));
+  if (numel(q_cat_out) == 0) return MLA_OK;
+  View3 r = view3(rope);
+  if (rope.shape[1] == 1) r.s1 = 0;  // one rope head broadcast to every head
+  r.n1 = H;
+  return cuda_status(launch_concat_q(dtype, view3(q_cat_out), view3(nope), r, (cudaStream_t)stream),
+                     "mla_concat_q");
+}
+
+mla_status mla_cache_write(mla_dtype dtype, mla_tensor cache, mla_tensor kv_c, mla_tensor k_pe,
+                           const int64_t* slot_mapping, int64_t num_tokens, void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens < 0");
+  MLA_TRY(check_view(kv_c, 2, "kv_c"));
+  MLA_TRY(check_view(k_pe, 2, "k_pe"));
+  const int64_t L = kv_c.shape[1], R = k_pe.shape[1];
+  MLA_TRY(check_cache(cache, L + R, "cache"));
+  if (kv_c.shape[0] != num_tokens || k_pe.shape[0] != num_tokens)
+    return fail(MLA_ERR_INVALID_ARG, "kv_c/k_pe rows (%lld/%lld) != num_tokens %lld",
+                (long long)kv_c.shape[0], (long long)k_pe.shape[0], (long long)num_tokens);
+  if (num_tokens == 0) return MLA_OK;
+  if (slot_mapping == nullptr) return fail(MLA_ERR_INVALID_ARG, "slot_mapping is null");
+  View3 kc{kv_c.data, kv_c.shape[0], 1, kv_c.shape[1], kv_c.stride[0], 0, 1};
+  View3 kp{k_pe.data, k_pe.shape[0], 1, k_pe.shape[1], k_pe.stride[0], 0, 1};
+  return cuda_status(launch_cache_write(dtype, view3(cache), kc, kp, L, R, slot_mapping, num_tokens,
+                                        (cudaStream_t)stream), "mla_cache_write");
+}
+
+size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank,
+                                 int32_t num_splits) {
+  if (batch < 0 || num_heads < 0 || kv_lora_rank < 0 || num_splits < 0) return 0;
+  return decode_ws_layout(batch, num_heads, kv_lora_rank, decode_units(num_splits)).total;
+}
+
+mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                      mla_tensor cache, const int32_t* block_table, int64_t block_table_stride,
+                      int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank,
+                      int32_t rope_dim, float softmax_scale, int32_t num_splits, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat, 3, "q_cat"));
+  MLA_TRY(check_view(o_lat_out, 3, "o_lat_out"));
+  const int64_t B = q_cat.shape[0], H = q_cat.shape[1];
+  const int64_t L = kv_lora_rank, R = rope_dim;
+  if (L <= 0 || R < 0) return fail(MLA_ERR_INVALID_ARG, "kv_lora_rank must be > 0 and rope_dim >= 0");
+  if (q_cat.shape[2] != L + R)
+    return fail(MLA_ERR_INVALID_ARG, "q_cat width %lld != L + R = %lld", (long long)q_cat.shape[2],
+                (long long)(L + R));
+  if (o_lat_out.shape[0] != B || o_lat_out.shape[1] != H || o_lat_out.shape[2] != L)
+    return fail(MLA_ERR_INVALID_ARG, "o_lat_out must be [B,H,L] = [%lld,%lld,%lld]", (long long)B,
+                (long long)H, (long long)L);
+  MLA_TRY(check_cache(cache, L + R, "cache"));
+  if (num_splits < 0) return fail(MLA_ERR_INVALID_ARG, "num_splits < 0");
+  if (B == 0 || H == 0) return MLA_OK;
+  if (B > INT32_MAX / 2 || H > 4096) return fail(MLA_ERR_UNSUPPORTED, "batch or head count too large");
+  if (block_table == nullptr || seq_lens == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "block_table and seq_lens must be non-null");
+  if (max_blocks <= 0 || block_table_stride < max_blocks)
+    return fail(MLA_ERR_INVALID_ARG, "need 0 < max_blocks <= block_table_stride");
+  if (L > 512) return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank %lld > 512", (long long)L);
+  if (L + R > 1024) return fail(MLA_ERR_UNSUPPORTED, "entry width %lld > 1024", (long long)(L + R));
+  const int32_t units = decode_units(num_splits);
+  const DecodeWsLayout lay = decode_ws_layout(B, H, L, units);
+  if (workspace == nullptr || workspace_bytes < lay.total)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes,
+                lay.total);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const DecodeSched s = decode_sched_from_ws(workspace, lay, (int32_t)B, units);
+  const CacheView cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
+                     (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
+  cudaStream_t st = (cudaStream_t)stream;
+  MLA_TRY(cuda_status(launch_decode_schedule(seq_lens, (int32_t)B, max_blocks, cv.page, s, st),
+                      "mla_decode schedule"));
+  MLA_TRY(cuda_status(launch_decode_simt(dtype, view3(o_lat_out), lse_out, view3(q_cat), cv,
+                                         block_table, block_table_stride, max_blocks, seq_lens,
+                                         (int32_t)B,
+                                         (int32_t)H, (int32_t)L, (int32_t)R, softmax_scale, s, st),
+                      "mla_decode split kernel"));
+  return cuda_status(launch_decode_combine(dtype, view3(o_lat_out), lse_out, seq_lens, (int32_t)B,
+                                           (int32_t)H, (int32_t)L, s, st),
+                     "mla_decode combine");
+}
+
+mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                       mla_tensor cache, const int32_t* block_table, int64_t block_table_stride,
+                       int32_t max_blocks, const int32_t* cu_seqlens_q, const int32_t* seq_lens_kv,
+                       int32_t batch, int32_t max_q_len, int32_t kv_lora_rank, int32_t rope_dim,
+                       float softmax_scale, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  g_msg[0] = 0;
+  (void)workspace;
+  (void)workspace_bytes;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat, 3, "q_cat"));
+  MLA_TRY(check_view(o_lat_out, 3, "o_lat_out"));
+  const int64_t T = q_cat.shape[0], H = q_cat.shape[1];
+  const int64_t L = kv_lora_rank, R = rope_dim;
+  if (L <= 0 || R < 0) return fail(MLA_ERR_INVALID_ARG, "kv_lora_rank must be > 0 and rope_dim >= 0");
+  if (q_cat.shape[2] != L + R) return fail(MLA_ERR_INVALID_ARG, "q_cat width != L + R");
+  if (o_lat_out.shape[0] != T || o_lat_out.shape[1] != H || o_lat_out.shape[2] != L)
+    return fail(MLA_ERR_INVALID_ARG, "o_lat_out must be [T,H,L]");
+  MLA_TRY(check_cache(cache, L + R, "cache"));
+  if (batch < 0 || max_q_len < 0) return fail(MLA_ERR_INVALID_ARG, "batch and max_q_len must be >= 0");
+  if (T == 0 || H == 0 || batch == 0) return MLA_OK;
+  if (T > INT32_MAX / 2 || H > 4096) return fail(MLA_ERR_UNSUPPORTED, "token or head count too large");
+  if (block_table == nullptr || cu_seqlens_q == nullptr || seq_lens_kv == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "block_table, cu_seqlens_q and seq_lens_kv must be non-null");
+  if (max_blocks <= 0 || block_table_stride < max_blocks)
+    return fail(MLA_ERR_INVALID_ARG, "need 0 < max_blocks <= block_table_stride");
+  if (L > 512) return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank %lld > 512", (long long)L);
+  if (L + R > 1024) return fail(MLA_ERR_UNSUPPORTED, "entry width > 1024");
+  const CacheView cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
+                     (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
+  return cuda_status(launch_prefill_simt(dtype, view3(o_lat_out), lse_out, view3(q_cat), cv,
+                                         block_table, block_table_stride, max_blocks, cu_seqlens_q,
+                                         seq_lens_kv, batch, (int32_t)T, (int32_t)H, (int32_t)L,
+                                         (int32_t)R, softmax_scale, (cudaStream_t)stream),
+                     "mla_prefill");
+}
+
+mla_status mla_device_error(void* stream) {
+  g_msg[0] = 0;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "mla_device_error: stream synchronize");
+  unsigned bits = copy_errors_read_clear() | attn_simt_errors_read_clear();
+  if (bits & kErrTimeout) return fail(MLA_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (bits & kErrDeviceData)
+    return fail(MLA_ERR_DEVICE_DATA, "a slot, block id or sequence length was out of range");
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Internal declarations shared by the translation units of libmla.so.
+// Nothing here is part of the C ABI (include/mla.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "mla.h"
+
+namespace mla {
+
+// Bits of the per-module device error words.
+constexpr unsigned kErrDeviceData = 1u;  // slot / block id / length out of range
+constexpr unsigned kErrTimeout = 2u;     // a bounded wait gave up
+
+// Keys per schedule tile of the split-KV decode (one page of 64 rows at page 64).
+constexpr int kTile = 64;
+
+// A rank-3 strided view in ELEMENTS (data already includes the storage offset).
+struct View3 {
+  void* data;
+  int64_t n0, n1, n2;
+  int64_t s0, s1, s2;
+};
+
+inline View3 view3(const mla_tensor& t) {
+  return View3{t.data, t.shape[0], t.shape[1], t.shape[2], t.stride[0], t.stride[1], t.stride[2]};
+}
+
+// The paged cache as the kernels see it.
+struct CacheView {
+  const void* data;  // element (blk, row, e) at data + blk*s_blk + row*s_row + e
+  int64_t s_blk, s_row;
+  int32_t num_blocks, page, entry;
+};
+
+// Decode schedule kept in the caller's workspace (all device pointers).
+struct DecodeSched {
+  int32_t* tile_prefix;  // [B+1] prefix sum of ceil(len_b / kTile)
+  int32_t* first_unit;   // [B]   work unit holding the first tile of b
+  int32_t* npieces;      // [B]   work units touching b (0 for an empty sequence)
+  int32_t* piece_base;   // [B]   first partial slot of b (if npieces[b] > 1)
+  float* part_o;         // [max_pieces, H, L] normalised partial outputs
+  float* part_lse;       // [max_pieces, H]    their natural-log LSE
+  int32_t units;         // number of work units W
+  int32_t max_pieces;    // B + W
+};
+
+// Workspace layout of mla_decode for (B, H, L, units).
+struct DecodeWsLayout {
+  size_t off_prefix, off_first, off_np, off_base, off_part_o, off_part_lse, total;
+};
+DecodeWsLayout decode_ws_layout(int64_t B, int64_t H, int64_t L, int64_t units);
+DecodeSched decode_sched_from_ws(void* ws, const DecodeWsLayout& lay, int32_t B, int32_t units);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// ---- launchers (return cudaSuccess or the launch error) -------------------
+cudaError_t launch_concat_q(mla_dtype dt, const View3& out, const View3& nope, const View3& rope,
+                            cudaStream_t st);
+cudaError_t launch_cache_write(mla_dtype dt, const View3& cache, const View3& kv_c,
+                               const View3& k_pe, int64_t L, int64_t R, const int64_t* slots,
+                               int64_t T, cudaStream_t st);
+cudaError_t launch_bmm_simt(mla_dtype dt, const View3& out, const View3& a, const View3& b,
+                            cudaStream_t st);
+
+cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
+                                   int32_t page, const DecodeSched& s, cudaStream_t st);
+cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
+                               const CacheView& cache, const int32_t* block_table,
+                               int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t H,
+                               int32_t L, int32_t R, float scale, const DecodeSched& s,
+                               cudaStream_t st);
+cudaError_t launch_decode_combine(mla_dtype dt, const View3& o_lat, float* lse,
+                                  const int32_t* seq_lens, int32_t B, int32_t H, int32_t L,
+                                  const DecodeSched& s, cudaStream_t st);
+cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
+                                const CacheView& cache, const int32_t* block_table,
+                                int64_t bt_stride, int32_t max_blocks, const int32_t* cu_q,
+                                const int32_t* kv_lens, int32_t B, int32_t T, int32_t H,
+                                int32_t L, int32_t R, float scale, cudaStream_t st);
+
+// Per-module error words: read and clear (after the stream was synchronised).
+unsigned copy_errors_read_clear();
+unsigned attn_simt_errors_read_clear();
+
+}  // namespace mla

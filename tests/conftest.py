@@ -26,3 +26,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def mla():
+    """The built library's binding (builds libmla.so in-tree if it is stale)."""
+    from mla_latent_kv_11_gb300 import build
+    build.build()
+    import mla_latent_kv_11_gb300 as m
+    m.lib()
+    return m

@@ -1,0 +1,109 @@
+"""The C ABI as seen from the host, without a GPU: the library loads, exports every
+entry point include/mla.h declares, and rejects malformed arguments before it
+touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mla():
+    from mla_latent_kv_11_gb300 import build
+    build.build()
+    import mla_latent_kv_11_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(mla):
+    names = declared_functions()
+    assert {"mla_absorb_q", "mla_concat_q", "mla_cache_write", "mla_decode", "mla_prefill",
+            "mla_v_up"} <= set(names)
+    lib = mla.lib()
+    for n in names:
+        assert hasattr(lib, n), f"libmla.so does not export {n}"
+    assert lib.mla_abi_version() == 1
+    assert lib.mla_status_string(2) == b"MLA_ERR_UNSUPPORTED"
+
+
+def _view(shape, strides, data=0x10000):
+    from mla_latent_kv_11_gb300 import MlaTensor
+    t = MlaTensor()
+    t.data = data
+    t.rank = len(shape)
+    for i, (n, s) in enumerate(zip(shape, strides)):
+        t.shape[i] = n
+        t.stride[i] = s
+    return t
+
+
+def _contig(shape, data=0x10000):
+    strides, acc = [], 1
+    for n in reversed(shape):
+        strides.insert(0, acc)
+        acc *= n
+    return _view(shape, strides, data)
+
+
+def test_bmm_rejects_malformed_operands_without_launching(mla):
+    # vllm.cpp BatchedMatmul: inner mismatch, batch mismatch, innermost stride != 1.
+    lib = mla.lib()
+    o = _contig([2, 3, 4])
+    assert lib.mla_absorb_q(1, o, _contig([2, 3, 4]), _contig([2, 5, 4]), None) == mla.MLA_ERR_INVALID_ARG
+    assert b"inner" in lib.mla_last_error()
+    assert lib.mla_absorb_q(1, o, _contig([2, 3, 4]), _contig([3, 4, 4]), None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_v_up(1, o, _view([2, 3, 4], [24, 8, 2]), _contig([2, 4, 4]), None) == mla.MLA_ERR_INVALID_ARG
+    assert b"innermost" in lib.mla_last_error()
+    assert lib.mla_v_up(7, o, _contig([2, 3, 4]), _contig([2, 4, 4]), None) == mla.MLA_ERR_INVALID_ARG
+    # empty work is fine and launches nothing
+    assert lib.mla_absorb_q(1, _contig([2, 0, 4]), _contig([2, 0, 4]), _contig([2, 4, 4]), None) == mla.MLA_OK
+
+
+def test_concat_and_cache_write_validation(mla):
+    lib = mla.lib()
+    assert lib.mla_concat_q(1, _contig([4, 8, 10]), _contig([4, 8, 8]), _contig([4, 8, 3]), None) \
+        == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_concat_q(1, _contig([4, 8, 10]), _contig([4, 8, 8]), _contig([4, 2, 2]), None) \
+        == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_concat_q(1, _contig([0, 8, 10]), _contig([0, 8, 8]), _contig([0, 8, 2]), None) == mla.MLA_OK
+    cache = _contig([4, 16, 10])
+    assert lib.mla_cache_write(1, cache, _contig([3, 8]), _contig([3, 2]), None, 3, None) \
+        == mla.MLA_ERR_INVALID_ARG                                 # null slot mapping
+    assert lib.mla_cache_write(1, cache, _contig([3, 8]), _contig([3, 3]), 0x1000, 3, None) \
+        == mla.MLA_ERR_INVALID_ARG                                 # entry width mismatch
+    assert lib.mla_cache_write(1, cache, _contig([0, 8]), _contig([0, 2]), None, 0, None) == mla.MLA_OK
+
+
+def test_decode_and_prefill_validation(mla):
+    lib = mla.lib()
+    B, H, L, R = 2, 16, 512, 64
+    q = _contig([B, H, L + R])
+    o = _contig([B, H, L])
+    cache = _contig([8, 64, L + R])
+    ok_args = dict(bt=0x2000, bts=4, mb=4, sl=0x3000)
+
+    def dec(o=o, q=q, cache=cache, L=L, R=R, bt=0x2000, bts=4, mb=4, sl=0x3000, ws=0x4000, wsb=1 << 30):
+        return lib.mla_decode(1, o, None, q, cache, bt, bts, mb, sl, L, R, 0.1, 0, ws, wsb, None)
+
+    assert dec(L=500) == mla.MLA_ERR_INVALID_ARG                   # q width != L + R
+    assert dec(o=_contig([B, H, L - 1])) == mla.MLA_ERR_INVALID_ARG
+    assert dec(cache=_contig([8, 64, 512])) == mla.MLA_ERR_INVALID_ARG
+    assert dec(bt=None) == mla.MLA_ERR_INVALID_ARG
+    assert dec(bts=2) == mla.MLA_ERR_INVALID_ARG                    # stride < max_blocks
+    assert dec(wsb=16) == mla.MLA_ERR_INVALID_ARG                   # workspace too small
+    assert b"workspace" in lib.mla_last_error()
+    assert dec(ws=0x4001) == mla.MLA_ERR_INVALID_ARG                # unaligned workspace
+    assert dec(q=_view([B, H, L + R], [H * (L + R), L + R, 2])) == mla.MLA_ERR_INVALID_ARG
+    assert dec(q=_contig([0, H, L + R]), o=_contig([0, H, L])) == mla.MLA_OK
+    assert lib.mla_prefill(1, o, None, q, cache, 0x2000, 4, 4, None, 0x3000, 2, 1, L, R, 0.1, None, 0,
+                           None) == mla.MLA_ERR_INVALID_ARG         # null cu_seqlens_q
+    del ok_args

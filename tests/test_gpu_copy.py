@@ -1,0 +1,125 @@
+"""Steps 2 and 3 on the GPU: q concat and paged cache write, bit-exact against the
+oracle's gathers, with NaN-poisoned outputs and sentinel-filled neighbours."""
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+from oracle import mla_oracle as orc
+from helpers import BF16_POISON, poisoned, to_dev, to_host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(x, dtype):
+    return mi.to_bf16_bits(x) if dtype == "bf16" else x.astype(np.float32)
+
+
+def _run_concat(mla, nope_t, rope_t, dtype):
+    import torch
+    T, H, L = nope_t.shape
+    R = rope_t.shape[2]
+    out = poisoned((T, H, L + R), dtype)
+    mla.mla_concat_q(out, nope_t, rope_t)
+    torch.cuda.synchronize()
+    return to_host_bits(out)
+
+
+def test_concat_unified_config_transposed_nope(mla):
+    # q_nope storage [N=128, B=64, 512] (the bmm output), viewed as its [64,128,512] transpose.
+    w = mi.write_concat_workload()
+    N, B, L = w.q_nope_storage.shape
+    store = to_dev(w.q_nope_storage, "bf16")
+    nope = store.as_strided((B, N, L), (L, B * L, 1))
+    assert not nope.is_contiguous()
+    rope = to_dev(w.q_pe, "bf16")
+    got = _run_concat(mla, nope, rope, "bf16")
+    nope_h = orc.strided_view(w.q_nope_storage.reshape(-1), 0, (B, N, L), (L, B * L, 1))
+    want = orc.concat_q(np.ascontiguousarray(nope_h), w.q_pe)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", ["contiguous_v3", "broadcast_rope", "nope_only", "odd_widths"])
+def test_concat_cases(mla, dtype, case):
+    T, H, L, R, Hr = {"contiguous_v3": (16, 128, 512, 64, 128), "broadcast_rope": (11, 16, 128, 64, 1),
+                      "nope_only": (5, 8, 512, 0, 8), "odd_widths": (7, 5, 13, 3, 5)}[case]
+    nope = _bits(mi.normal(55, T * H * L), dtype).reshape(T, H, L)
+    rope = _bits(mi.normal(66, T * Hr * R), dtype).reshape(T, Hr, R)
+    if dtype == "bf16" and nope.size > 4:
+        nope.reshape(-1)[1] = 0x8000          # -0
+        nope.reshape(-1)[3] = 0x7FC1          # a NaN payload
+    got = _run_concat(mla, to_dev(nope, dtype), to_dev(rope, dtype), dtype)
+    want = orc.concat_q(nope, rope)
+    if dtype == "f32":
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    else:
+        assert np.array_equal(got, want)
+
+
+def _unified(nb, n_layers, page, E, fill=0x1234):
+    import torch
+    return torch.full((nb, n_layers * page * E), fill, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+
+
+def test_cache_write_unified_slot_view_no_bleed(mla):
+    import torch
+    w = mi.write_concat_workload()
+    nb, page, E, n_layers, layer = w.num_blocks, w.page, w.entry, w.n_layers, w.layer
+    L = w.kv_c.shape[1]
+    kv_c, k_pe = to_dev(w.kv_c, "bf16"), to_dev(w.k_pe, "bf16")
+    slots = torch.from_numpy(w.slots).cuda()
+    big = _unified(nb, n_layers, page, E)
+    flat = big.view(-1)
+    view = flat.as_strided((nb, page, E), (n_layers * page * E, E, 1), layer * page * E)
+    assert view.stride(0) == 110592 and view.storage_offset() == 36864
+    mla.mla_cache_write(view, kv_c, k_pe, slots)
+    # the contiguous per-layer reference through the same kernel
+    ref = torch.zeros((nb, page, E), dtype=torch.bfloat16, device="cuda")
+    mla.mla_cache_write(ref, kv_c, k_pe, slots)
+    mla.mla_device_error()
+    got = to_host_bits(flat)
+    want = orc.cache_write(np.full(nb * n_layers * page * E, 0x1234, np.uint16), layer * page * E, nb,
+                           page, (n_layers * page * E, E, 1), w.kv_c, w.k_pe, w.slots)
+    assert np.array_equal(got, want)                                  # rows and neighbours, bit for bit
+    written = np.zeros(nb * page, bool)
+    written[w.slots] = True
+    v = got.reshape(nb, n_layers, page, E)[:, layer].reshape(nb * page, E)
+    assert np.array_equal(v[written], to_host_bits(ref).reshape(nb * page, E)[written])
+    del L
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_cache_write_padding_odd_widths_and_out_of_range(mla, dtype):
+    import torch
+    nb, page, L, R = 6, 16, 13, 3                          # odd widths: element path
+    E, T = L + R, 40
+    kv = _bits(mi.normal(1, T * L), dtype).reshape(T, L)
+    kp = _bits(mi.normal(2, T * R), dtype).reshape(T, R)
+    slots = mi.permutation(3, nb * page)[:T].copy()
+    slots[4] = -1                                           # padding
+    cache = to_dev(_bits(np.full(nb * page * E, 0.5, np.float32), dtype), dtype).view(nb, page, E)
+    mla.mla_cache_write(cache, to_dev(kv, dtype), to_dev(kp, dtype), torch.from_numpy(slots).cuda())
+    mla.mla_device_error()
+    want = orc.cache_write(_bits(np.full(nb * page * E, 0.5, np.float32), dtype), 0, nb, page,
+                           (page * E, E, 1), kv, kp, slots)
+    got = to_host_bits(cache).reshape(-1)
+    assert np.array_equal(got.view(np.uint16) if dtype == "bf16" else got.view(np.uint32),
+                          want.view(np.uint16) if dtype == "bf16" else want.view(np.uint32))
+    # a slot past the cache writes nothing and is reported
+    bad = torch.tensor([nb * page + 3, 0], dtype=torch.int64, device="cuda")
+    before = to_host_bits(cache).copy()
+    mla.mla_cache_write(cache, to_dev(kv[:2], dtype), to_dev(kp[:2], dtype), bad)
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_device_error()
+    assert e.value.status == mla.MLA_ERR_DEVICE_DATA
+    after = to_host_bits(cache)
+    row0 = after.reshape(nb * page, E)[0]                   # slot 0 took token 1's row
+    assert np.array_equal(row0[:L], kv[1]) and np.array_equal(row0[L:], kp[1])
+    mask = np.ones(nb * page, bool)
+    mask[0] = False
+    assert np.array_equal(after.reshape(nb * page, E)[mask], before.reshape(nb * page, E)[mask])
+    mla.mla_device_error()                                  # the error word was cleared
+
+
+def test_poison_constant_is_the_pages():
+    assert BF16_POISON == 0x7FC0

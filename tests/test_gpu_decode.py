@@ -1,0 +1,138 @@
+"""Step 4 (decode) on the GPU: paged split-KV decode with LSE combine against the
+float64 oracle, on the V2-Lite fp32 and V3 bf16 workloads, the shrunk memra
+geometries, degenerate lengths, several split counts, a unified-slot cache view
+(bit-identical to the contiguous cache) and the full-size variable-length batch
+on sampled sequences."""
+import math
+
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+from oracle import mla_oracle as orc
+from helpers import check_close, poisoned, to_dev, to_f64, to_host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_cache(cache_bits, dtype, layout, n_layers=3, layer=1, fill_seed=999):
+    """The cache on the device, contiguous or as one layer of a unified block-major slot."""
+    import torch
+    nb, page, E = cache_bits.shape
+    if layout == "contiguous":
+        return to_dev(cache_bits, dtype), None
+    other = mi.encode(mi.draw("normal", fill_seed, nb * n_layers * page * E, 0.1), dtype)
+    big = to_dev(other, dtype).view(nb, n_layers, page, E)
+    big[:, layer].copy_(to_dev(cache_bits, dtype))
+    view = big[:, layer]
+    assert not view.is_contiguous() and view.stride(0) == n_layers * page * E
+    return view, big
+
+
+def run_decode(mla, q_bits, cache_bits, table, lens, dtype, L, R, scale, num_splits=0,
+               layout="contiguous"):
+    import torch
+    B, H, E = q_bits.shape
+    cache, keep = _device_cache(cache_bits, dtype, layout)
+    q = to_dev(q_bits, dtype)
+    o = poisoned((B, H, L), dtype)
+    lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
+    mla.mla_decode(o, q, cache, torch.from_numpy(np.ascontiguousarray(table, np.int32)).cuda(),
+                   torch.from_numpy(np.asarray(lens, np.int32)).cuda(), L, R, scale, lse_out=lse,
+                   num_splits=num_splits)
+    mla.mla_device_error()
+    del keep
+    return o, lse.cpu().numpy().astype(np.float64)
+
+
+def oracle_decode(q_bits, cache_bits, table, lens, dtype, L, R, scale, ids=None):
+    nb, page, E = cache_bits.shape
+    storage = mi.decode_f64(cache_bits.reshape(-1), dtype)
+    return orc.decode(mi.decode_f64(q_bits, dtype), storage, 0, page, (page * E, E, 1), L, R,
+                      np.asarray(table), np.asarray(lens), scale, batch_ids=ids)
+
+
+def check_lse(got, want):
+    fin = np.isfinite(want)
+    assert np.array_equal(np.isfinite(got), fin)
+    if fin.any():
+        assert np.max(np.abs(got[fin] - want[fin])) < 1e-3
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 3, 7])
+def test_decode_v2_lite_fp32(mla, num_splits):
+    w = mi.v2_lite_decode()
+    g = w.geom
+    q = mi.encode(mi.draw("uniform", 11, w.batch * g.n_head * g.entry), "f32").reshape(w.batch, g.n_head, g.entry)
+    o, lse = run_decode(mla, q, w.full_cache(), w.block_table, w.seq_lens, "f32", g.kv_rank, g.d_rope,
+                        w.scale, num_splits)
+    want, want_lse = oracle_decode(q, w.full_cache(), w.block_table, w.seq_lens, "f32", g.kv_rank,
+                                   g.d_rope, w.scale)
+    check_close(to_f64(o), want, "f32", f"v2-lite decode splits={num_splits}")
+    check_lse(lse, want_lse)
+
+
+@pytest.mark.parametrize("sharp", [1.0, 30.0])
+def test_decode_v3_bf16_and_view_bit_identity(mla, sharp):
+    w = mi.v3_decode_small()
+    g = w.geom
+    q = mi.encode(mi.draw("normal", 1011, w.batch * g.n_head * g.entry, 0.1 * sharp), "bf16").reshape(
+        w.batch, g.n_head, g.entry)
+    args = (q, w.full_cache(), w.block_table, w.seq_lens, "bf16", g.kv_rank, g.d_rope, w.scale)
+    o, lse = run_decode(mla, *args)
+    want, want_lse = oracle_decode(*args)
+    info = check_close(to_f64(o), want, "bf16", f"v3 decode x{sharp}")
+    check_lse(lse, want_lse)
+    o_view, lse_view = run_decode(mla, *args, layout="unified")
+    assert np.array_equal(to_host_bits(o_view), to_host_bits(o))      # strided view: same bits
+    assert np.array_equal(lse_view, lse)
+    o2, _ = run_decode(mla, *args)
+    assert np.array_equal(to_host_bits(o2), to_host_bits(o))          # run to run: same bits
+    del info
+
+
+@pytest.mark.parametrize("dims", [(4, 24, 8, 32, 64), (3, 12, 4, 20, 48), (4, 32, 0, 32, 64)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_small_geometries_ragged_lengths(mla, dims, dtype):
+    H, P, R, V, L = dims
+    E = L + R
+    lens = [0, 1, 2, 63, 64, 65, 200, 1000, 5]
+    page = 16
+    need = [(n + page - 1) // page for n in lens]
+    nb = sum(need) + 3
+    perm = mi.permutation(70, nb)
+    table = np.full((len(lens), max(need) + 2), -7, np.int32)      # unused entries are garbage
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    cache = mi.encode(mi.draw("uniform", 71, nb * page * E), dtype).reshape(nb, page, E)
+    q = mi.encode(mi.draw("uniform", 72, len(lens) * H * E, 2.0), dtype).reshape(len(lens), H, E)
+    scale = 1.0 / math.sqrt(P + R)
+    for splits in (0, 1, 5, 64):
+        o, lse = run_decode(mla, q, cache, table, lens, dtype, L, R, scale, splits)
+        want, want_lse = oracle_decode(q, cache, table, lens, dtype, L, R, scale)
+        check_close(to_f64(o), want, dtype, f"dims {dims} splits {splits}")
+        check_lse(lse, want_lse)
+        got = to_f64(o)
+        assert np.all(got[0] == 0) and np.all(lse[0] == -np.inf)      # empty sequence
+        row0 = mi.decode_f64(cache[table[1, 0], 0, :L], dtype)
+        assert np.array_equal(got[1], np.broadcast_to(row0, (H, L)))  # one row: that row, exactly
+
+
+def test_decode_large_variable_lengths_sampled(mla):
+    # B=64 sequences of 1K..16K rows, auto split count (the bench configuration), sampled check.
+    w = mi.v3_decode_large(materialize_cache=True)
+    g = w.geom
+    q = mi.encode(mi.draw("normal", 3011, w.batch * g.n_head * g.entry, 0.1), "bf16").reshape(
+        w.batch, g.n_head, g.entry)
+    o, lse = run_decode(mla, q, w.full_cache(), w.block_table, w.seq_lens, "bf16", g.kv_rank,
+                        g.d_rope, w.scale)
+    got = to_f64(o)
+    assert np.all(np.isfinite(got))
+    lens = w.seq_lens
+    ids = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 0, 31, w.batch - 1})
+    want, want_lse = oracle_decode(q, w.full_cache(), w.block_table, lens, "bf16", g.kv_rank,
+                                   g.d_rope, w.scale, ids=ids)
+    check_close(got[ids], want, "bf16", "large decode (sampled sequences)")
+    check_lse(lse[ids], want_lse)
