@@ -164,13 +164,17 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lo
  *   (including its own queries' rows).
  *   Query i of sequence b sits at position p = seq_lens_kv[b] - q_len_b + i and
  *   attends rows 0..p (bottom-right causal alignment); otherwise as mla_decode.
- *   max_q_len bounds q_len_b. No workspace is needed: pass NULL and 0. */
+ *   max_q_len bounds q_len_b. workspace: device scratch of at least
+ *   mla_prefill_workspace_size(batch) bytes, 256-byte aligned, caller-owned. */
 mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
                        mla_tensor cache, const int32_t* block_table, int64_t block_table_stride,
                        int32_t max_blocks, const int32_t* cu_seqlens_q, const int32_t* seq_lens_kv,
                        int32_t batch, int32_t max_q_len, int32_t kv_lora_rank, int32_t rope_dim,
                        float softmax_scale, void* workspace, size_t workspace_bytes,
                        void* stream);
+
+/* Bytes of workspace mla_prefill needs for `batch` sequences. */
+size_t mla_prefill_workspace_size(int32_t batch);
 
 /* Step 5 - W_UV un-projection ([vt] BatchedMatmul at the _v_up_proj call site: a
  * (B,N,L) -> (N,B,L) transposed input, output written into a transposed (B,N,V);

@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
             "mla_decode_workspace_size": ([I32, I32, I32, I32], SZ),
             "mla_prefill": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, P, I32, I32, I32, I32, F32, P,
                              SZ, P], ctypes.c_int),
+            "mla_prefill_workspace_size": ([I32], SZ),
             "mla_v_up": ([ctypes.c_int, T, T, T, P], ctypes.c_int),
             "mla_device_error": ([P], ctypes.c_int),
         }
@@ -178,8 +179,12 @@ def mla_decode(o_lat_out, q_cat, cache, block_table, seq_lens, kv_lora_rank: int
                             _stream(stream)))
 
 
+def mla_prefill_workspace_size(batch: int) -> int:
+    return int(lib().mla_prefill_workspace_size(batch))
+
+
 def mla_prefill(o_lat_out, q_cat, cache, block_table, cu_seqlens_q, seq_lens_kv, max_q_len: int,
-                kv_lora_rank: int, rope_dim: int, softmax_scale: float, lse_out=None,
+                kv_lora_rank: int, rope_dim: int, softmax_scale: float, lse_out=None, workspace=None,
                 stream=None) -> None:
     """Step 4 (prefill): causal attention of many queries per sequence over the paged cache."""
     import torch
@@ -188,12 +193,15 @@ def mla_prefill(o_lat_out, q_cat, cache, block_table, cu_seqlens_q, seq_lens_kv,
         raise MlaError(MLA_ERR_INVALID_ARG, "cu_seqlens_q must be contiguous int32")
     if lse_out is not None and (lse_out.dtype != torch.float32 or not lse_out.is_contiguous()):
         raise MlaError(MLA_ERR_INVALID_ARG, "lse_out must be contiguous float32")
+    if workspace is None:
+        workspace = torch.empty(mla_prefill_workspace_size(seq_lens_kv.numel()), dtype=torch.uint8,
+                                device=q_cat.device)
     _check(lib().mla_prefill(_dtype_code(o_lat_out, q_cat, cache), as_mla_tensor(o_lat_out),
                              _ptr(lse_out), as_mla_tensor(q_cat), as_mla_tensor(cache),
                              block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
                              cu_seqlens_q.data_ptr(), seq_lens_kv.data_ptr(), seq_lens_kv.numel(),
-                             max_q_len, kv_lora_rank, rope_dim, softmax_scale, None, 0,
-                             _stream(stream)))
+                             max_q_len, kv_lora_rank, rope_dim, softmax_scale, workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def mla_v_up(out, o_lat, w_uv, stream=None) -> None:

@@ -266,27 +266,41 @@ mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla
     return fail(MLA_ERR_INVALID_ARG, "need 0 < max_blocks <= block_table_stride");
   if (L > 512) return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank %lld > 512", (long long)L);
   if (L + R > 1024) return fail(MLA_ERR_UNSUPPORTED, "entry width %lld > 1024", (long long)(L + R));
-  const int32_t units = decode_units(num_splits);
-  const DecodeWsLayout lay = decode_ws_layout(B, H, L, units);
+  const DecodeWsLayout lay = decode_ws_layout(B, H, L, decode_units(num_splits));
   if (workspace == nullptr || workspace_bytes < lay.total)
     return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes,
                 lay.total);
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  const DecodeSched s = decode_sched_from_ws(workspace, lay, (int32_t)B, units);
   const CacheView cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
                      (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
+  const View3 qv = view3(q_cat), ov = view3(o_lat_out);
+  const bool tc = tc_attention_supported(dtype, (int)H, (int)L, (int)R, true, cv, qv, ov);
+  // work units: one per 2-CTA cluster on the tensor-core path, else from num_splits
+  const int32_t units = tc ? tc_decode_units(num_splits) : decode_units(num_splits);
+  const DecodeSched s = decode_sched_from_ws(workspace, lay, (int32_t)B, units);
   cudaStream_t st = (cudaStream_t)stream;
   MLA_TRY(cuda_status(launch_decode_schedule(seq_lens, (int32_t)B, max_blocks, cv.page, s, st),
                       "mla_decode schedule"));
-  MLA_TRY(cuda_status(launch_decode_simt(dtype, view3(o_lat_out), lse_out, view3(q_cat), cv,
-                                         block_table, block_table_stride, max_blocks, seq_lens,
-                                         (int32_t)B,
-                                         (int32_t)H, (int32_t)L, (int32_t)R, softmax_scale, s, st),
-                      "mla_decode split kernel"));
-  return cuda_status(launch_decode_combine(dtype, view3(o_lat_out), lse_out, seq_lens, (int32_t)B,
-                                           (int32_t)H, (int32_t)L, s, st),
+  if (tc) {
+    MLA_TRY(cuda_status(launch_decode_tc(ov, lse_out, qv, cv, block_table, block_table_stride,
+                                         max_blocks, seq_lens, (int32_t)B, (int32_t)H, (int32_t)L,
+                                         (int32_t)R, softmax_scale, s, st),
+                        "mla_decode split kernel (tensor cores)"));
+  } else {
+    MLA_TRY(cuda_status(launch_decode_simt(dtype, ov, lse_out, qv, cv, block_table,
+                                           block_table_stride, max_blocks, seq_lens, (int32_t)B,
+                                           (int32_t)H, (int32_t)L, (int32_t)R, softmax_scale, s, st),
+                        "mla_decode split kernel"));
+  }
+  return cuda_status(launch_decode_combine(dtype, ov, lse_out, seq_lens, (int32_t)B, (int32_t)H,
+                                           (int32_t)L, s, st),
                      "mla_decode combine");
+}
+
+size_t mla_prefill_workspace_size(int32_t batch) {
+  if (batch < 0) return 0;
+  return ((size_t)(batch + 1) * sizeof(int32_t) + 255) & ~size_t(255);
 }
 
 mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
@@ -296,8 +310,6 @@ mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, ml
                        float softmax_scale, void* workspace, size_t workspace_bytes,
                        void* stream) {
   g_msg[0] = 0;
-  (void)workspace;
-  (void)workspace_bytes;
   MLA_TRY(check_dtype(dtype));
   MLA_TRY(check_view(q_cat, 3, "q_cat"));
   MLA_TRY(check_view(o_lat_out, 3, "o_lat_out"));
@@ -317,12 +329,24 @@ mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, ml
     return fail(MLA_ERR_INVALID_ARG, "need 0 < max_blocks <= block_table_stride");
   if (L > 512) return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank %lld > 512", (long long)L);
   if (L + R > 1024) return fail(MLA_ERR_UNSUPPORTED, "entry width > 1024");
+  if (workspace == nullptr || workspace_bytes < mla_prefill_workspace_size(batch))
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes,
+                mla_prefill_workspace_size(batch));
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   const CacheView cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
                      (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
-  return cuda_status(launch_prefill_simt(dtype, view3(o_lat_out), lse_out, view3(q_cat), cv,
-                                         block_table, block_table_stride, max_blocks, cu_seqlens_q,
-                                         seq_lens_kv, batch, (int32_t)T, (int32_t)H, (int32_t)L,
-                                         (int32_t)R, softmax_scale, (cudaStream_t)stream),
+  const View3 qv = view3(q_cat), ov = view3(o_lat_out);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (tc_attention_supported(dtype, (int)H, (int)L, (int)R, false, cv, qv, ov))
+    return cuda_status(launch_prefill_tc(ov, lse_out, qv, cv, block_table, block_table_stride,
+                                         max_blocks, cu_seqlens_q, seq_lens_kv, batch, (int32_t)H,
+                                         (int32_t)L, (int32_t)R, softmax_scale,
+                                         static_cast<int32_t*>(workspace), st),
+                       "mla_prefill (tensor cores)");
+  return cuda_status(launch_prefill_simt(dtype, ov, lse_out, qv, cv, block_table, block_table_stride,
+                                         max_blocks, cu_seqlens_q, seq_lens_kv, batch, (int32_t)T,
+                                         (int32_t)H, (int32_t)L, (int32_t)R, softmax_scale, st),
                      "mla_prefill");
 }
 
@@ -330,7 +354,7 @@ mla_status mla_device_error(void* stream) {
   g_msg[0] = 0;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "mla_device_error: stream synchronize");
-  unsigned bits = copy_errors_read_clear() | attn_simt_errors_read_clear();
+  unsigned bits = copy_errors_read_clear() | attn_simt_errors_read_clear() | attn_tc_errors_read_clear();
   if (bits & kErrTimeout) return fail(MLA_ERR_TIMEOUT, "a bounded device-side wait gave up");
   if (bits & kErrDeviceData)
     return fail(MLA_ERR_DEVICE_DATA, "a slot, block id or sequence length was out of range");

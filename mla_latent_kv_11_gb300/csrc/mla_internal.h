@@ -82,8 +82,24 @@ cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, co
                                 const int32_t* kv_lens, int32_t B, int32_t T, int32_t H,
                                 int32_t L, int32_t R, float scale, cudaStream_t st);
 
+// Tensor-core attention (attn_tc.cu): bf16, L = 512, R in {0, 64}, 16-byte
+// aligned views; decode needs H = 128, prefill H in {64, 128}.
+bool tc_attention_supported(mla_dtype dt, int H, int L, int R, bool decode, const CacheView& cv,
+                            const View3& q, const View3& o);
+int tc_decode_units(int num_splits);
+cudaError_t launch_decode_tc(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
+                             const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t B, int32_t H, int32_t L, int32_t R,
+                             float scale, const DecodeSched& s, cudaStream_t st);
+cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
+                              const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                              const int32_t* cu_q, const int32_t* kv_lens, int32_t B, int32_t H,
+                              int32_t L, int32_t R, float scale, int32_t* item_prefix,
+                              cudaStream_t st);
+
 // Per-module error words: read and clear (after the stream was synchronised).
 unsigned copy_errors_read_clear();
 unsigned attn_simt_errors_read_clear();
+unsigned attn_tc_errors_read_clear();
 
 }  // namespace mla
