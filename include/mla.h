@@ -184,6 +184,29 @@ size_t mla_prefill_workspace_size(int32_t batch);
 mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tensor w_uv,
                     void* stream);
 
+/* Bytes of the static scratch behind mla_decode_noalloc (40 MiB). */
+#define MLA_DECODE_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
+
+/* mla_decode without a workspace, for callers that cannot allocate device
+ * memory: code running inside another framework's memory pool, plugins whose
+ * host forbids cudaMalloc on the hot path (it synchronises the device and can
+ * fail under memory pressure), runtimes that reserve all device memory up
+ * front. The source pages have no counterpart of this call.
+ *   Arguments, results and errors are those of mla_decode minus the workspace.
+ *   The split-KV scratch lives in a static device array of
+ *   MLA_DECODE_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ *   until the process exits; a batch whose scratch would not fit (about
+ *   (B + work units) * H * L * 4 bytes) returns MLA_ERR_UNSUPPORTED. The call
+ *   allocates nothing. Its first call on a device looks up the array's device
+ *   address (once per device); make that first call before any stream capture.
+ *   All calls share the array: calls whose kernels overlap on the GPU race and
+ *   must be serialised by the caller. */
+mla_status mla_decode_noalloc(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out,
+                              mla_tensor q_cat, mla_tensor cache, const int32_t* block_table,
+                              int64_t block_table_stride, int32_t max_blocks,
+                              const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim,
+                              float softmax_scale, int32_t num_splits, void* stream);
+
 /* Synchronises `stream`, then reports and clears the device-side error words the
  * kernels set (out-of-range slot, block id or length: MLA_ERR_DEVICE_DATA; a
  * bounded wait that gave up: MLA_ERR_TIMEOUT). MLA_OK if none was set. */

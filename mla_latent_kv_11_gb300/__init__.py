@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
                              SZ, P], ctypes.c_int),
             "mla_prefill_workspace_size": ([I32], SZ),
             "mla_v_up": ([ctypes.c_int, T, T, T, P], ctypes.c_int),
+            "mla_decode_noalloc": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, I32, P],
+                                   ctypes.c_int),
             "mla_device_error": ([P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
@@ -208,6 +210,23 @@ def mla_v_up(out, o_lat, w_uv, stream=None) -> None:
     """Step 5: out[h,b,:] = o_lat[h,b,:] @ w_uv[h] (views [H,B,V], [H,B,L], [H,L,V])."""
     _check(lib().mla_v_up(_dtype_code(out, o_lat, w_uv), as_mla_tensor(out), as_mla_tensor(o_lat),
                           as_mla_tensor(w_uv), _stream(stream)))
+
+
+def mla_decode_noalloc(o_lat_out, q_cat, cache, block_table, seq_lens, kv_lora_rank: int,
+                       rope_dim: int, softmax_scale: float, lse_out=None, num_splits: int = 0,
+                       stream=None) -> None:
+    """mla_decode for callers that cannot allocate device memory: no workspace, the
+    scratch is a fixed array inside the library (shared by all calls; do not overlap
+    calls on the GPU)."""
+    import torch
+    _check_int32_table(block_table, seq_lens)
+    if lse_out is not None and (lse_out.dtype != torch.float32 or not lse_out.is_contiguous()):
+        raise MlaError(MLA_ERR_INVALID_ARG, "lse_out must be contiguous float32")
+    _check(lib().mla_decode_noalloc(_dtype_code(o_lat_out, q_cat, cache), as_mla_tensor(o_lat_out),
+                                    _ptr(lse_out), as_mla_tensor(q_cat), as_mla_tensor(cache),
+                                    block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
+                                    seq_lens.data_ptr(), kv_lora_rank, rope_dim, softmax_scale,
+                                    num_splits, _stream(stream)))
 
 
 def mla_device_error(stream=None) -> None:

@@ -96,6 +96,18 @@ mla_status check_cache(const mla_tensor& cache, int64_t E, const char* name) {
 
 }  // namespace
 
+mla_status report_status(mla_status st, const char* fmt, ...) {
+  if (st == MLA_OK || fmt == nullptr) {
+    g_msg[0] = 0;
+    return st;
+  }
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
 DecodeWsLayout decode_ws_layout(int64_t B, int64_t H, int64_t L, int64_t units) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   DecodeWsLayout l{};

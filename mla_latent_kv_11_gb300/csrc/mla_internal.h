@@ -97,6 +97,9 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
                               int32_t L, int32_t R, float scale, int32_t* item_prefix,
                               cudaStream_t st);
 
+// Set (or clear, with MLA_OK) the calling thread's mla_last_error() message.
+mla_status report_status(mla_status st, const char* fmt, ...);
+
 // Per-module error words: read and clear (after the stream was synchronised).
 unsigned copy_errors_read_clear();
 unsigned attn_simt_errors_read_clear();
