@@ -6,26 +6,46 @@
 // M dimension of every MMA; keys come in tiles of 64 cache rows. The output
 // accumulator O is 128 x 512 fp32, which alone would fill a CTA's 512 TMEM
 // columns, so a cluster of two CTAs shares each row tile:
-//   CTA 0 owns latent columns   0..255            (Q, K and V boxes 0..3)
-//   CTA 1 owns latent columns 256..511 + the rope (Q, K and V boxes 4..7, 8)
-// Each CTA loads only its columns of every cache row (the row is read from
-// HBM once per pair), computes its partial scores S_r = Q_r K_r^T (M=128,
-// N=64), hands them to the peer through distributed shared memory, and both
-// form S = S_0 + S_1 in the same order, so both run the identical online
-// softmax. Each CTA then accumulates its own half O_r += P V_r (M=128, N=256,
-// K=64) in TMEM: no MMA is duplicated and no cache byte is read twice.
+//   CTA 0 owns latent columns   0..255
+//   CTA 1 owns latent columns 256..511 and the 64 rope columns
+// Each CTA TMA-loads only its columns of every cache row (a row crosses HBM
+// once per pair), computes its partial scores S_r = Q_r K_r^T, and the pair
+// swaps partials so both hold S = S_0 + S_1 (summed in the same order) and run
+// the identical online softmax. Each CTA then accumulates its half
+// O_r += P V_r. No MMA is duplicated and no cache byte is read twice.
 //
-// Roles (256 threads per CTA): warp 0 issues TMA loads, warp 1 issues MMAs,
-// warp 2 owns the TMEM allocation, warps 4..7 run the softmax, the O rescale
-// and the epilogue, one thread per query row (TMEM lane). Stages are tracked
-// with mbarriers; every wait is bounded in time and a timeout winds the
-// kernel down and reports MLA_ERR_TIMEOUT instead of hanging.
+// Memory plan per CTA. Tensor memory holds everything the MMAs reuse:
+//   O half [0,256) fp32 | S [256,320) fp32 | P [320,352) bf16 pairs |
+//   Q half [352, 352 + 128 or 160) bf16 pairs,
+// so both MMAs take their A operand from TMEM and shared memory only streams
+// the B operand (the cache tile). Shared memory holds 3 (rope) or 4 (NoPE)
+// cache-tile stages and two outgoing and two incoming exchange slots.
 //
-// Softmax is evaluated in base 2 with the scale folded in. The running max is
-// updated lazily: O and the denominator are only rescaled when the max grows
-// by more than 2^8, so exponentials stay below 256 and the result is exact
-// up to rounding. P is rounded to bf16 for the PV MMA and the denominator sums
-// the rounded values.
+// Exchange. The SM-to-SM network moves only about 10 bytes per clock each way,
+// so the pair does not swap fp32 partial scores (32 KB per tile) but
+// exponentials: each CTA takes its row maximum c_r of x_r = s_r * scale * log2 e
+// and sends E_r = 2^(x_r - c_r) in bf16 with c_r (16.5 KB per tile). Since
+//   2^(x_0 + x_1 - m) = E_0 * E_1 * 2^(c_0 + c_1 - m),
+// both CTAs form the same P from the same bf16 operands in the same order;
+// c_0 + c_1 bounds the row maximum from above, so nothing can overflow, and
+// the extra rounding is that of the bf16 P the PV MMA takes anyway. A
+// dedicated exchange warpgroup reads S out of TMEM as soon as the MMA has
+// produced it, computes c and E and pushes them with one bulk copy (completion
+// counted in bytes on the peer's barrier); the softmax warpgroup combines the
+// two halves concurrently.
+//
+// Roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs (a polling
+// state machine that issues whichever of QK(g+1) and PV(g) is ready), warp 2
+// owns the TMEM allocation, warps 4..7 load Q into TMEM and run the exchange,
+// warps 8..11 run the softmax, the O rescale and the epilogue, one thread per
+// query row (TMEM lane) in each group; warp 3 forwards the softmax group's
+// "incoming buffer read" signals to the peer (a cluster-scope release stalls
+// the issuing thread for about a microsecond, so it is kept off the softmax). Every wait is bounded in time; a
+// timeout winds the kernel down and reports MLA_ERR_TIMEOUT instead of hanging.
+//
+// The running reference maximum is updated lazily (O and the denominator are
+// rescaled only when the bound c_0 + c_1 grows by more than 2^8, so P stays
+// below 256). P is rounded to bf16 for the PV MMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -45,42 +65,69 @@ using namespace ptx;
 
 __device__ unsigned g_tc_err = 0;
 
-constexpr int kRows = 128;          // M: query rows per tile
-constexpr int kKeysT = 64;          // keys per tile
-constexpr int kBoxBytesQ = kRows * 128;   // one 64-column box of the row tile (16 KB)
+constexpr int kRows = 128;                // M: query rows per tile
+constexpr int kKeysT = 64;                // keys per tile
 constexpr int kBoxBytesK = kKeysT * 128;  // one 64-column box of a key tile (8 KB)
-constexpr int kThreads = 256;
-constexpr int kSoftmaxWarp0 = 4;
+constexpr int kESlotBytes = kRows * kKeysT * 2;   // E = 2^(s - c) of one tile, bf16 (16 KB)
+constexpr int kXSlot = kESlotBytes + kRows * 4;     // + the rows' maxima c (16.5 KB)
+constexpr int kThreads = 384;
+constexpr int kXchgWarp0 = 4;             // exchange warpgroup: warps 4..7
+constexpr int kSoftmaxWarp0 = 8;          // softmax warpgroup: warps 8..11
+constexpr int kSoftmaxBar = 1;            // named barrier of the softmax warpgroup
+constexpr int kXchgBar = 2;               // named barrier of the exchange warpgroup
 constexpr float kLazyRescale = 8.0f;      // log2 units
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;            // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;          // S buffers: [256, 320) and [320, 384)
+constexpr uint32_t kTmemO = 0;
+constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemP = 320;
+constexpr uint32_t kTmemQ = 352;
 
 template <int kRope>
 struct Cfg {
-  static constexpr int kBoxes = 4 + kRope / 64;      // boxes per CTA (max over ranks)
-  static constexpr int kStages = kRope ? 2 : 3;
-  static constexpr int kQBytes = kBoxes * kBoxBytesQ;
+  static constexpr int kBoxes = 4 + kRope / 64;      // boxes per CTA (max over the pair)
+  static constexpr int kStages = kRope ? 3 : 4;
   static constexpr int kStageBytes = kBoxes * kBoxBytesK;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kOffQ + kQBytes;
-  static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-  static constexpr int kOffX = kOffP + 2 * kRows * 128;
-  static constexpr int kOffBar = kOffX + kRows * kKeysT * 4;
+  static constexpr int kOffKV = 0;
+  static constexpr int kOffXloc = kOffKV + kStages * kStageBytes;   // own E + c, 2 slots
+  static constexpr int kOffXrem = kOffXloc + 2 * kXSlot;            // the peer's, 2 slots
+  static constexpr int kOffBar = (kOffXrem + 2 * kXSlot + 127) & ~127;
   static constexpr int kBarBytes = 1024;
   static constexpr int kSmem = kOffBar + kBarBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;    // slack for 1 KB alignment
 };
 
 struct Bars {
-  uint64_t q_full, seg_done, o_empty, mma_final;
-  uint64_t kv_full[3], kv_empty[3];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[2], pv_done[2];
-  uint64_t x_full, x_empty;
+  uint64_t kv_full[4], kv_empty[4];
+  uint64_t s_full, s_empty, p_full, pv_done;
+  uint64_t seg_done, o_empty, q_ready, mma_final;
+  uint64_t x_full[2], x_empty[2];
+  uint64_t own_ready[2]; // own E and c of the tile are in outgoing slot b
+  uint64_t xloc_free[2]; // the softmax group has read outgoing slot b
+  uint64_t xin_free[2];  // the softmax group has read incoming slot b
   uint32_t tmem_base;
   int abort_flag;
 };
+
+#ifdef MLA_TRACE
+// Cycle stamps of pipeline events of work unit 0, for tuning builds only.
+__device__ long long g_trace[2][8][512];
+__device__ long long g_trace2[2][8][512];
+#define MLA_TRACE_AT(ev, g)                                              \
+  do {                                                                    \
+    if (unit == 0 && (g) < 512) g_trace[rank][ev][(g)] = clock64();      \
+  } while (0)
+#define MLA_TRACE2_AT(ev, g)                                                          \
+  do {                                                                                 \
+    if (unit == 0 && row == 0 && (g) < 512) g_trace2[rank][ev][(g)] = clock64();      \
+  } while (0)
+#else
+#define MLA_TRACE_AT(ev, g) \
+  do {                      \
+  } while (0)
+#define MLA_TRACE2_AT(ev, g) \
+  do {                       \
+  } while (0)
+#endif
 
 struct Seg {
   int b;      // sequence
@@ -96,6 +143,9 @@ struct TcParams {
   int H, tpt;        // heads, tokens per row tile (128 / H)
   int L, R;
   float scale_log2;
+  // queries [tokens, H, L+R]
+  const __nv_bfloat16* q;
+  int64_t q_s0, q_s1;
   // output
   __nv_bfloat16* o_lat;
   int64_t o_s0, o_s1;
@@ -199,22 +249,17 @@ __device__ __forceinline__ void set_abort(Bars& bars, uint32_t peer) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(1) : "memory");
 }
 
-// 16-byte chunk `c` of row `r` in a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
 template <int kRope>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
-                       const TcParams p) {
+    mla_attn_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const TcParams p) {
   using C = Cfg<kRope>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + C::kOffBar);
-  unsigned char* sQ = smem + C::kOffQ;
   unsigned char* sKV = smem + C::kOffKV;
-  unsigned char* sP = smem + C::kOffP;
-  float* sX = reinterpret_cast<float*>(smem + C::kOffX);
+  unsigned char* sXloc = smem + C::kOffXloc;   // [2] x (E [128 rows x 128 B, chunk-swizzled] | c [128])
+  unsigned char* sXrem = smem + C::kOffXrem;   // same layout, written by the peer
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
@@ -224,61 +269,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int col0 = rank == 0 ? 0 : 256;
 
   if (tid == 0) {
-    mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.seg_done, 1);
-    mbar_init(&bars.o_empty, 128);
-    mbar_init(&bars.mma_final, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
     }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_empty, 4);
+    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.pv_done, 1);
+    mbar_init(&bars.seg_done, 1);
+    mbar_init(&bars.o_empty, 4);
+    mbar_init(&bars.q_ready, 4);
+    mbar_init(&bars.mma_final, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_empty[i], 128);
-      mbar_init(&bars.p_full[i], 128);
-      mbar_init(&bars.pv_done[i], 1);
+      mbar_init(&bars.x_full[i], 1);
+      mbar_init(&bars.x_empty[i], 1);
+      mbar_init(&bars.own_ready[i], 4);
+      mbar_init(&bars.xloc_free[i], 1);
+      mbar_init(&bars.xin_free[i], 1);
     }
-    mbar_init(&bars.x_full, 128);
-    mbar_init(&bars.x_empty, 128);
     bars.abort_flag = 0;
     fence_mbar_init();
+    // the incoming buffers of tiles 0 and 1 are armed before the peer can send
+    mbar_arrive_expect_tx(&bars.x_full[0], kXSlot);
+    mbar_arrive_expect_tx(&bars.x_full[1], kXSlot);
   }
   if (warp == 2) {
     tmem_alloc(&bars.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&qmap);
-    tma_prefetch_desc(&kvmap);
-  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&kvmap);
   tc_fence_before();
-  cluster_sync();   // barriers of both CTAs initialised before any remote arrive
+  cluster_sync();   // barriers of both CTAs initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (cache tiles)
     Walker wk;
     wk.init(p, unit, nunits);
     Seg sg;
-    int gt = 0, seg_i = 0;
-    int issued_q = 0;
-    int issued[3] = {0, 0, 0};
+    int gt = 0;
+    int issued[4] = {0, 0, 0, 0};
     bool ok = true;
     const int rows_box = min(p.page, kKeysT);
     const int subs = kKeysT / rows_box;
     while (ok && wk.next(p, sg)) {
-      if (lane == 0) {
-        if (seg_i > 0) ok = mbar_wait(&bars.seg_done, (seg_i - 1) & 1, abort);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars.q_full, nbox * kBoxBytesQ);
-          for (int c = 0; c < nbox; ++c)
-            tma_load_3d(sQ + c * kBoxBytesQ, &qmap, &bars.q_full, col0 + 64 * c, 0, sg.tok0);
-          ++issued_q;
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       const int nt = ntiles(sg);
       const int32_t* bt = p.block_table + (int64_t)sg.b * p.bt_stride;
       for (int j0 = 0; ok && j0 < nt; j0 += 32) {
@@ -291,10 +328,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane == 0 && ok) {
             const int s = gt % C::kStages;
             ok = mbar_wait(&bars.kv_empty[s], ((gt / C::kStages) & 1) ^ 1, abort);
+            MLA_TRACE_AT(0, gt);
             if (ok) {
               const int kt = sg.k0 + (j0 + jj) * kKeysT;
               unsigned char* dst = sKV + s * C::kStageBytes;
-              // gather the (block, row) pieces of this tile that hold rows < k1
               int blks[8], rows0[8], nsub = 0;
               if (subs == 1) {
                 blks[0] = blk1;
@@ -332,13 +369,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
       }
-      ++seg_i;
     }
     if (!ok && lane == 0) set_abort(bars, peer);
-    // never leave with copies in flight: wait for the last phase of every barrier we loaded into
+    // never leave with copies in flight: wait for the last phase of every stage loaded
     if (lane == 0) {
       volatile int dummy = 0;
-      if (issued_q > 0) mbar_wait(&bars.q_full, (issued_q - 1) & 1, &dummy);
       for (int s = 0; s < C::kStages; ++s)
         if (issued[s] > 0) mbar_wait(&bars.kv_full[s], (issued[s] - 1) & 1, &dummy);
     }
@@ -352,51 +387,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t id_qk = idesc_bf16(kRows, kKeysT, false, false);
       const uint32_t id_pv = idesc_bf16(kRows, 256, false, true);
-      const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
-      auto issue_pv = [&](int g, bool first) -> bool {
-        const int pb = g & 1;
-        if (!mbar_wait(&bars.p_full[pb], (g >> 1) & 1, abort)) return false;
-        tc_fence_after();
-        const int s = g % C::kStages;
-        const uint32_t vb = kv_base + s * C::kStageBytes;
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = sdesc_sw128(p_base + pb * kRows * 128 + kk * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(vb + kk * 16 * 128, kBoxBytesK, 1024);
-          umma_bf16(tmem + kTmemO, a, b, id_pv, (first && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(&bars.kv_empty[s]);
-        umma_commit(&bars.pv_done[pb]);
-        return true;
-      };
+      const uint32_t kv_base = smem_u32(sKV);
       while (ok && wk.next(p, sg)) {
-        ok = mbar_wait(&bars.q_full, seg_i & 1, abort);
         const int nt = ntiles(sg);
-        for (int j = 0; ok && j < nt; ++j) {
-          const int g = gt + j;
-          const int s = g % C::kStages, sb = g & 1;
-          ok = mbar_wait(&bars.kv_full[s], (g / C::kStages) & 1, abort) &&
-               mbar_wait(&bars.s_empty[sb], ((g >> 1) & 1) ^ 1, abort);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kb = kv_base + s * C::kStageBytes;
-          for (int c = 0; c < nbox; ++c)
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = sdesc_sw128(q_base + c * kBoxBytesQ + kk * 32, 16, 1024);
-              const uint64_t b = sdesc_sw128(kb + c * kBoxBytesK + kk * 32, 16, 1024);
-              umma_bf16(tmem + kTmemS + sb * kKeysT, a, b, id_qk, (c | kk) ? 1u : 0u);
+        ok = mbar_wait(&bars.q_ready, seg_i & 1, abort);
+        int qk = 0, pv = 0;
+        uint64_t last = globaltimer_ns();
+        uint32_t spins = 0;
+        while (ok && pv < nt) {
+          bool did = false;
+          if (qk < nt) {
+            const int t = gt + qk, s = t % C::kStages;
+            // S is single-buffered: QK(t) needs S(t-1) read out by the softmax group
+            if (mbar_poll(&bars.kv_full[s], (t / C::kStages) & 1) && mbar_poll(&bars.s_empty, (t & 1) ^ 1)) {
+              MLA_TRACE_AT(1, t);
+              tc_fence_after();
+              const uint32_t kb = kv_base + s * C::kStageBytes;
+              for (int c = 0; c < nbox; ++c)
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + c * 32 + kk * 8,
+                               sdesc_sw128(kb + c * kBoxBytesK + kk * 32, 16, 1024), id_qk, (c | kk) ? 1u : 0u);
+              umma_commit(&bars.s_full);
+              ++qk;
+              did = true;
             }
-          umma_commit(&bars.s_full[sb]);
-          if (j > 0) {
-            if (j == 1 && seg_i > 0) ok = mbar_wait(&bars.o_empty, (seg_i - 1) & 1, abort);
-            ok = ok && issue_pv(g - 1, j == 1);
+          }
+          if (pv < qk) {
+            const int t = gt + pv, s = t % C::kStages;
+            const bool o_free = pv > 0 || seg_i == 0 || mbar_poll(&bars.o_empty, (seg_i - 1) & 1);
+            if (o_free && mbar_poll(&bars.p_full, t & 1)) {
+              MLA_TRACE_AT(2, t);
+              tc_fence_after();
+              const uint32_t vb = kv_base + s * C::kStageBytes;
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16_ta(tmem + kTmemO, tmem + kTmemP + kk * 8, sdesc_sw128(vb + kk * 16 * 128, kBoxBytesK, 1024),
+                             id_pv, (pv > 0 || kk > 0) ? 1u : 0u);
+              umma_commit(&bars.kv_empty[s]);
+              umma_commit(&bars.pv_done);
+              if (pv == nt - 1) umma_commit(&bars.seg_done);
+              ++pv;
+              did = true;
+            }
+          }
+          if (did) {
+            spins = 0;
+            last = globaltimer_ns();
+          } else {
+            __nanosleep(32);   // leave the issue slots to the softmax warps
+            if ((++spins & 255u) == 0 && (*abort || globaltimer_ns() - last > kWaitLimitNs)) ok = false;
           }
         }
-        if (ok && nt > 0) {
-          if (nt == 1 && seg_i > 0) ok = mbar_wait(&bars.o_empty, (seg_i - 1) & 1, abort);
-          ok = ok && issue_pv(gt + nt - 1, nt == 1);
-        }
         if (!ok) break;
-        umma_commit(&bars.seg_done);
+        if (nt == 0) umma_commit(&bars.seg_done);
         gt += nt;
         ++seg_i;
       }
@@ -406,13 +448,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       volatile int dummy = 0;
       mbar_wait(&bars.mma_final, 0, &dummy);
     }
-  } else if (warp >= kSoftmaxWarp0) {
-    // ------------------------------------------------------------ softmax / epilogue
-    const int row = tid - kSoftmaxWarp0 * 32;               // 0..127 == TMEM lane
-    const uint32_t lane_addr = (uint32_t)((warp - kSoftmaxWarp0) * 32) << 16;
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ forwarder: releases the
+    // incoming buffers to the peer once the softmax group has read them
+    if (lane == 0) {
+      Walker wk;
+      wk.init(p, unit, nunits);
+      Seg sg;
+      int gt = 0;
+      bool ok = true;
+      while (ok && wk.next(p, sg)) {
+        const int nt = ntiles(sg);
+        for (int j = 0; ok && j < nt; ++j) {
+          const int t = gt + j, b = t & 1;
+          ok = mbar_wait(&bars.xin_free[b], (t >> 1) & 1, abort);
+          if (ok) mbar_arrive_remote(&bars.x_empty[b], peer);
+        }
+        gt += nt;
+      }
+      if (!ok) set_abort(bars, peer);
+    }
+  } else if (warp >= kXchgWarp0 && warp < kXchgWarp0 + 4) {
+    // ------------------------------------------------------------ exchange group: Q load;
+    // per tile: S out of TMEM, own row max c and E = 2^(s*scale - c) in bf16, pushed to the peer
+    const int row = tid - kXchgWarp0 * 32;                  // 0..127 == TMEM lane
+    const uint32_t lane_addr = (uint32_t)((warp - kXchgWarp0) * 32) << 16;
     const int t_in_tile = row / p.H, head = row - t_in_tile * p.H;
-    const uint32_t peer_x = map_to_rank(sX + row * kKeysT, peer);
-    float* my_x = sX + row * kKeysT;
+    const uint32_t peer_rem0 = map_to_rank(sXrem, peer);
+    const uint32_t peer_xfull0 = map_to_rank(&bars.x_full[0], peer);
+    // A named barrier has no timeout, so every decision is taken by all 128 threads.
+    auto group_all = [](bool v) { return named_bar_and(kXchgBar, 128, v); };
     Walker wk;
     wk.init(p, unit, nunits);
     Seg sg;
@@ -422,90 +487,177 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nt = ntiles(sg);
       const bool row_valid = row < p.H * p.tpt && t_in_tile < sg.ntok;
       const int limit = row_valid ? min(sg.k1, sg.pos0 + t_in_tile + 1) : 0;
-      float m = -CUDART_INF_F, l = 0.f;
-      for (int j = 0; ok && j < nt; ++j) {
-        const int g = gt + j, sb = g & 1, pb = g & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[sb], (g >> 1) & 1, abort));
+      // ---- this CTA's Q columns of the row tile into TMEM, once the previous
+      // segment's MMAs are done (two bf16 per column, the even one low)
+      if (seg_i > 0) {
+        ok = group_all(mbar_wait(&bars.seg_done, (seg_i - 1) & 1, abort));
         if (!ok) break;
         tc_fence_after();
-        float sp[64];
-        tmem_ld32(tmem + lane_addr + kTmemS + sb * kKeysT, *reinterpret_cast<float(*)[32]>(sp));
-        tmem_ld32(tmem + lane_addr + kTmemS + sb * kKeysT + 32, *reinterpret_cast<float(*)[32]>(sp + 32));
+      }
+      {
+        const __nv_bfloat16* qrow = p.q + (int64_t)(sg.tok0 + t_in_tile) * p.q_s0 + (int64_t)head * p.q_s1 + col0;
+        for (int c = 0; c < nbox; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row_valid) w = *reinterpret_cast<const uint4*>(qrow + c * 64 + i * 8);
+            v[4 * i] = w.x;
+            v[4 * i + 1] = w.y;
+            v[4 * i + 2] = w.z;
+            v[4 * i + 3] = w.w;
+          }
+          tmem_st32u(tmem + lane_addr + kTmemQ + c * 32, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.q_ready);
+      }
+      for (int j = 0; ok && j < nt; ++j) {
+        const int t = gt + j, b = t & 1;
+        // ---- S(t) out of TMEM; the MMA may then compute S(t+1)
+        ok = group_all(mbar_wait(&bars.s_full, t & 1, abort));
+        if (!ok) break;
+        MLA_TRACE_AT(3, t);
+        tc_fence_after();
+        float sv[64];
+        tmem_ld32(tmem + lane_addr + kTmemS, *reinterpret_cast<float(*)[32]>(sv));
+        tmem_ld32(tmem + lane_addr + kTmemS + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&bars.s_empty[sb]);
-        // exchange partial scores with the peer
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(&bars.x_empty, (g & 1) ^ 1, abort));
-        if (!ok) break;
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) st_cluster_v4(peer_x + c * 4, sp[c], sp[c + 1], sp[c + 2], sp[c + 3]);
-        mbar_arrive_remote(&bars.x_full, peer);
-        ok = __all_sync(0xffffffffu, mbar_wait<true>(&bars.x_full, g & 1, abort));
-        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.s_empty);
+        // ---- own row max c (base 2, scale folded in) and E = 2^(x - c) in bf16
         const int kbase = sg.k0 + j * kKeysT;
-        float mx = -CUDART_INF_F;
+        float c = -CUDART_INF_F;
+        if (__all_sync(0xffffffffu, kbase + kKeysT <= limit)) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 o = *reinterpret_cast<const float4*>(my_x + c);
-          // S = S_rank0 + S_rank1 in both CTAs
-          const float x0 = rank == 0 ? sp[c] + o.x : o.x + sp[c];
-          const float x1 = rank == 0 ? sp[c + 1] + o.y : o.y + sp[c + 1];
-          const float x2 = rank == 0 ? sp[c + 2] + o.z : o.z + sp[c + 2];
-          const float x3 = rank == 0 ? sp[c + 3] + o.w : o.w + sp[c + 3];
-          sp[c] = kbase + c < limit ? x0 * p.scale_log2 : -CUDART_INF_F;
-          sp[c + 1] = kbase + c + 1 < limit ? x1 * p.scale_log2 : -CUDART_INF_F;
-          sp[c + 2] = kbase + c + 2 < limit ? x2 * p.scale_log2 : -CUDART_INF_F;
-          sp[c + 3] = kbase + c + 3 < limit ? x3 * p.scale_log2 : -CUDART_INF_F;
-          mx = fmaxf(mx, fmaxf(fmaxf(sp[c], sp[c + 1]), fmaxf(sp[c + 2], sp[c + 3])));
+          for (int k = 0; k < 64; ++k) c = fmaxf(c, sv[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            sv[k] = kbase + k < limit ? sv[k] : -CUDART_INF_F;
+            c = fmaxf(c, sv[k]);
+          }
         }
-        mbar_arrive_remote(&bars.x_empty, peer);   // my receive buffer is free again
-        // lazy online softmax
+        c = c == -CUDART_INF_F ? -CUDART_INF_F : c * p.scale_log2;
+        const float neg_c = c == -CUDART_INF_F ? 0.f : -c;
+        uint32_t ek[32];
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(ex2_approx(fmaf(sv[k], p.scale_log2, neg_c)),
+                                                         ex2_approx(fmaf(sv[k + 1], p.scale_log2, neg_c)));
+          ek[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        // ---- into the outgoing slot b once the softmax group and the last push are done with it
+        ok = group_all(mbar_wait(&bars.xloc_free[b], ((t >> 1) & 1) ^ 1, abort));
+        if (!ok) break;
+        if (row == 0) bulk_wait_read_all();
+        named_bar(kXchgBar, 128);
+        unsigned char* slot = sXloc + b * kXSlot;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(slot + row * 128 + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(ek[4 * ch], ek[4 * ch + 1], ek[4 * ch + 2], ek[4 * ch + 3]);
+        reinterpret_cast<float*>(slot + kESlotBytes)[row] = c;
+        fence_proxy_async_smem();
+        named_bar(kXchgBar, 128);
+        MLA_TRACE_AT(4, t);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.own_ready[b]);
+        bool sent = true;
+        if (row == 0) {
+          // the peer's incoming slot b is free once it has consumed tile t - 2
+          sent = mbar_wait<true>(&bars.x_empty[b], ((t >> 1) & 1) ^ 1, abort);
+          if (sent) {
+            bulk_copy_to_peer(peer_rem0 + b * kXSlot, slot, kXSlot, peer_xfull0 + b * 8);
+            bulk_commit_group();
+          }
+        }
+        ok = group_all(sent);
+      }
+      if (!ok) break;
+      gt += nt;
+      ++seg_i;
+    }
+    if (!ok) set_abort(bars, peer);
+    if (row == 0) bulk_wait_read_all();
+  } else if (warp >= kSoftmaxWarp0) {
+    // ------------------------------------------------------------ softmax group: P, O rescale, epilogue
+    const int row = tid - kSoftmaxWarp0 * 32;               // 0..127 == TMEM lane
+    const uint32_t lane_addr = (uint32_t)((warp - kSoftmaxWarp0) * 32) << 16;
+    const int t_in_tile = row / p.H, head = row - t_in_tile * p.H;
+    auto group_all = [](bool v) { return named_bar_and(kSoftmaxBar, 128, v); };
+    Walker wk;
+    wk.init(p, unit, nunits);
+    Seg sg;
+    int gt = 0, seg_i = 0;
+    bool ok = true;
+    while (ok && wk.next(p, sg)) {
+      const int nt = ntiles(sg);
+      const bool row_valid = row < p.H * p.tpt && t_in_tile < sg.ntok;
+      float m = -CUDART_INF_F, l = 0.f;    // running reference max (base 2) and denominator
+      for (int j = 0; ok && j < nt; ++j) {
+        const int g = gt + j, b = g & 1;
+        ok = group_all(mbar_wait(&bars.own_ready[b], (g >> 1) & 1, abort) &&
+                       mbar_wait<true>(&bars.x_full[b], (g >> 1) & 1, abort));
+        if (!ok) break;
+        const unsigned char* own = sXloc + b * kXSlot;
+        const unsigned char* rem = sXrem + b * kXSlot;
+        uint4 eo[8], er[8];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          eo[ch] = *reinterpret_cast<const uint4*>(own + row * 128 + ((ch ^ (row & 7)) << 4));
+          er[ch] = *reinterpret_cast<const uint4*>(rem + row * 128 + ((ch ^ (row & 7)) << 4));
+        }
+        const float c_own = reinterpret_cast<const float*>(own + kESlotBytes)[row];
+        const float c_rem = reinterpret_cast<const float*>(rem + kESlotBytes)[row];
+        // both slots are read: re-arm the incoming one, release it to the peer (through
+        // warp 3) and hand the outgoing one back to the exchange group
+        named_bar(kSoftmaxBar, 128);
+        if (row == 0) {
+          mbar_arrive_expect_tx(&bars.x_full[b], kXSlot);
+          mbar_arrive(&bars.xin_free[b]);
+          mbar_arrive(&bars.xloc_free[b]);
+        }
+        // ---- tile upper bound M = c_0 + c_1 (same order in both CTAs); lazy reference max
+        const float c0 = rank == 0 ? c_own : c_rem, c1 = rank == 0 ? c_rem : c_own;
+        const float M = (c0 == -CUDART_INF_F || c1 == -CUDART_INF_F) ? -CUDART_INF_F : c0 + c1;
         float alpha = 1.f;
         bool rescale_o = false;
-        if (mx > m + kLazyRescale || (m == -CUDART_INF_F && mx > -CUDART_INF_F)) {
-          alpha = m == -CUDART_INF_F ? 0.f : exp2f(m - mx);
+        if (M > m + kLazyRescale || (m == -CUDART_INF_F && M > -CUDART_INF_F)) {
+          alpha = m == -CUDART_INF_F ? 0.f : ex2_approx(m - M);
           rescale_o = (m != -CUDART_INF_F) && j > 0;
-          m = mx;
+          m = M;
         }
+        const float factor = M == -CUDART_INF_F ? 0.f : ex2_approx(M - m);
+        // ---- P = E_0 * E_1 * 2^(M - m): identical operands and order in both CTAs
+        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(rank == 0 ? eo : er);
+        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(rank == 0 ? er : eo);
         float sum = 0.f;
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float e0 = m == -CUDART_INF_F ? 0.f : exp2f(sp[c] - m);
-          const float e1 = m == -CUDART_INF_F ? 0.f : exp2f(sp[c + 1] - m);
-          const __nv_bfloat162 h = __floats2bfloat162_rn(e0, e1);
-          const float2 hf = __bfloat1622float2(h);
-          sum += hf.x + hf.y;
-          pk[c >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int k = 0; k < 32; ++k) {
+          const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w0[k]));
+          const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1[k]));
+          const float p0 = (a0.x * a1.x) * factor, p1 = (a0.y * a1.y) * factor;
+          sum += p0 + p1;
+          const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&h);
         }
         l = l * alpha + sum;
-        // the P buffer was last read by PV(g - 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.pv_done[pb], ((g >> 1) & 1) ^ 1, abort));
-        if (!ok) break;
-        unsigned char* prow = sP + pb * kRows * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + sw128(row, c)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        // rows of a partial tile past the sequence: zero their V so garbage cannot reach O
-        const int nvalid = sg.k1 - kbase;
-        if (nvalid < kKeysT) {
-          unsigned char* st = sKV + (g % C::kStages) * C::kStageBytes;
-          const int nz = (kKeysT - nvalid) * 8 * 4;       // 16-byte chunks in 4 latent boxes
-          for (int i = row; i < nz; i += 128) {
-            const int box = i / ((kKeysT - nvalid) * 8);
-            const int rem = i - box * ((kKeysT - nvalid) * 8);
-            const int r = nvalid + rem / 8, c = rem & 7;
-            *reinterpret_cast<uint4*>(st + box * kBoxBytesK + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-          }
+        MLA_TRACE_AT(7, g);
+        // ---- P(g) replaces P(g-1) in TMEM once PV(g-1) is done; O is rescaled then too
+        if (g > 0) {
+          ok = group_all(mbar_wait(&bars.pv_done, (g - 1) & 1, abort));
+          if (!ok) break;
         }
+        MLA_TRACE_AT(5, g);
+        tc_fence_after();
         // tcgen05.ld/st are warp-collective: the whole warp rescales if any of its rows must
         if (__any_sync(0xffffffffu, rescale_o)) {
           const float f = rescale_o ? alpha : 1.f;
-          // O must hold PV(g-1) before it is scaled
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort));
-          if (!ok) break;
-          tc_fence_after();
           for (int c = 0; c < 256; c += 32) {
             float v[32];
             tmem_ld32(tmem + lane_addr + kTmemO + c, v);
@@ -514,15 +666,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) v[i] *= f;
             tmem_st32(tmem + lane_addr + kTmemO + c, v);
           }
-          tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tmem_st32u(tmem + lane_addr + kTmemP, pk);
+        // rows of a partial tile past the sequence: zero their V so garbage cannot reach O
+        const int kbase = sg.k0 + j * kKeysT;
+        const int nvalid = sg.k1 - kbase;
+        if (nvalid < kKeysT) {
+          unsigned char* st = sKV + (g % C::kStages) * C::kStageBytes;
+          const int per_box = (kKeysT - nvalid) * 8;         // 16-byte chunks per latent box
+          for (int i = row; i < 4 * per_box; i += 128) {
+            const int box = i / per_box, rem_i = i - box * per_box;
+            *reinterpret_cast<uint4*>(st + box * kBoxBytesK + (nvalid + rem_i / 8) * 128 + (rem_i & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars.p_full[pb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full);
+        MLA_TRACE_AT(6, g);
       }
       if (!ok) break;
-      // epilogue: O / l for this CTA's 256 columns
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.seg_done, seg_i & 1, abort));
+      // ---- epilogue: O / l for this CTA's 256 columns
+      ok = group_all(mbar_wait(&bars.seg_done, seg_i & 1, abort));
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -568,7 +735,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars.o_empty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.o_empty);
       gt += nt;
       ++seg_i;
     }
@@ -658,13 +826,12 @@ int max_clusters() {
 }
 
 template <int kRope>
-cudaError_t launch_tc(const TcParams& p, const CUtensorMap& qm, const CUtensorMap& km, int clusters,
-                      cudaStream_t st) {
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap& km, int clusters, cudaStream_t st) {
   using C = Cfg<kRope>;
   cudaError_t e = cudaFuncSetAttribute(mla_attn_tc_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  mla_attn_tc_kernel<kRope><<<dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st>>>(qm, km, p);
+  mla_attn_tc_kernel<kRope><<<dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st>>>(km, p);
   return cudaGetLastError();
 }
 
@@ -691,14 +858,15 @@ int tc_decode_units(int num_splits) {
 
 static cudaError_t run_tc(mla_dtype, TcParams& p, const View3& q, const CacheView& cv, int clusters,
                           cudaStream_t st) {
-  CUtensorMap qm, km;
+  CUtensorMap km;
   const int E = p.L + p.R;
-  if (!make_map3d(&qm, q.data, E, p.H, q.n0, (uint64_t)q.s1 * 2, (uint64_t)q.s0 * 2, 64, p.H, p.tpt))
-    return cudaErrorInvalidValue;
+  p.q = static_cast<const __nv_bfloat16*>(q.data);
+  p.q_s0 = q.s0;
+  p.q_s1 = q.s1;
   if (!make_map3d(&km, cv.data, E, cv.page, cv.num_blocks, (uint64_t)cv.s_row * 2, (uint64_t)cv.s_blk * 2, 64,
                   cv.page < 64 ? cv.page : 64, 1))
     return cudaErrorInvalidValue;
-  return p.R == 64 ? launch_tc<64>(p, qm, km, clusters, st) : launch_tc<0>(p, qm, km, clusters, st);
+  return p.R == 64 ? launch_tc<64>(p, km, clusters, st) : launch_tc<0>(p, km, clusters, st);
 }
 
 cudaError_t launch_decode_tc(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
@@ -759,6 +927,13 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
   const int clusters = R == 64 ? max_clusters<64>() : max_clusters<0>();
   return run_tc(MLA_BF16, p, q, cache, clusters, st);
 }
+
+#ifdef MLA_TRACE
+extern "C" int mla_debug_trace(long long* host) {
+  const int e = (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
+  return e ? e : (int)cudaMemcpyFromSymbol(host + 2 * 8 * 512, g_trace2, sizeof(g_trace2));
+}
+#endif
 
 unsigned attn_tc_errors_read_clear() {
   unsigned v = 0, zero = 0;

@@ -107,7 +107,7 @@ extern "C" mla_status mla_decode_noalloc(mla_dtype dtype, mla_tensor o_lat_out, 
   const CacheView cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
                      (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
   const View3 qv = view3(q_cat), ov = view3(o_lat_out);
-  const bool tc = tc_attention_supported(dtype, (int)H, (int)L, (int)R, true, cv, qv, ov);
+  const bool tc = softmax_scale > 0.f && tc_attention_supported(dtype, (int)H, (int)L, (int)R, true, cv, qv, ov);
   const int32_t units = tc ? tc_decode_units(num_splits)
                            : (num_splits > 0 ? num_splits : 2 * device_sm_count());
   const DecodeWsLayout lay = decode_ws_layout(B, H, L, units);

@@ -287,7 +287,7 @@ mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla
   const CacheView cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
                      (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
   const View3 qv = view3(q_cat), ov = view3(o_lat_out);
-  const bool tc = tc_attention_supported(dtype, (int)H, (int)L, (int)R, true, cv, qv, ov);
+  const bool tc = softmax_scale > 0.f && tc_attention_supported(dtype, (int)H, (int)L, (int)R, true, cv, qv, ov);
   // work units: one per 2-CTA cluster on the tensor-core path, else from num_splits
   const int32_t units = tc ? tc_decode_units(num_splits) : decode_units(num_splits);
   const DecodeSched s = decode_sched_from_ws(workspace, lay, (int32_t)B, units);
@@ -350,7 +350,7 @@ mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, ml
                      (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
   const View3 qv = view3(q_cat), ov = view3(o_lat_out);
   cudaStream_t st = (cudaStream_t)stream;
-  if (tc_attention_supported(dtype, (int)H, (int)L, (int)R, false, cv, qv, ov))
+  if (softmax_scale > 0.f && tc_attention_supported(dtype, (int)H, (int)L, (int)R, false, cv, qv, ov))
     return cuda_status(launch_prefill_tc(ov, lse_out, qv, cv, block_table, block_table_stride,
                                          max_blocks, cu_seqlens_q, seq_lens_kv, batch, (int32_t)H,
                                          (int32_t)L, (int32_t)R, softmax_scale,
