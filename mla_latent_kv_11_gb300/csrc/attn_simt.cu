@@ -30,7 +30,6 @@ __device__ unsigned g_attn_err = 0;
 constexpr int kHeads = 16;    // heads per CTA
 constexpr int kKeys = 32;     // keys per inner tile
 constexpr int kThreads = 256;
-constexpr int kMaxL = 512;    // latent columns per thread pair: 2 * 256
 
 __device__ __forceinline__ float ld(const float* p) { return *p; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -308,40 +307,78 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
 }
 
 // Merge the partials of every sequence cut across several units; write o = 0
-// and lse = -inf for empty sequences. One CTA per (sequence, head).
+// and lse = -inf for empty sequences. One warp per (sequence, head); each lane
+// combines 16-byte chunks of the rows with weights e^(lse_i - max).
+template <typename T>
+__device__ __forceinline__ void store4(T* o, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* o, float4 v) {
+  *reinterpret_cast<float4*>(o) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* o, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&a);
+  w.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(o) = w;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128) decode_combine_kernel(
     T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
     int B, int H, int L, DecodeSched s) {
-  const int b = blockIdx.x, h = blockIdx.y;
+  const int b = blockIdx.x;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (h >= H) return;
   const int np = s.npieces[b];
   if (np == 1) return;
   T* o = o_lat + (int64_t)b * o_s0 + (int64_t)h * o_s1;
   if (np == 0) {
-    for (int c = threadIdx.x; c < L; c += blockDim.x) st(o + c, 0.f);
-    if (threadIdx.x == 0 && lse_out) lse_out[(int64_t)b * H + h] = -CUDART_INF_F;
+    for (int c = lane; c < L; c += 32) st(o + c, 0.f);
+    if (lane == 0 && lse_out) lse_out[(int64_t)b * H + h] = -CUDART_INF_F;
     return;
   }
   const int base = s.piece_base[b];
+  const float* lse_p = s.part_lse + (int64_t)base * H + h;
+  const int64_t pstride = (int64_t)H * L;
   float m = -CUDART_INF_F;
-  for (int i = 0; i < np; ++i) m = fmaxf(m, s.part_lse[(int64_t)(base + i) * H + h]);
+  for (int i = 0; i < np; ++i) m = fmaxf(m, lse_p[(int64_t)i * H]);
   float tot = 0.f;
   for (int i = 0; i < np; ++i) {
-    const float li = s.part_lse[(int64_t)(base + i) * H + h];
+    const float li = lse_p[(int64_t)i * H];
     tot += li == -CUDART_INF_F ? 0.f : __expf(li - m);
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  for (int c = threadIdx.x; c < L; c += blockDim.x) {
-    float v = 0.f;
-    for (int i = 0; i < np; ++i) {
-      const float li = s.part_lse[(int64_t)(base + i) * H + h];
-      const float wgt = li == -CUDART_INF_F ? 0.f : __expf(li - m);
-      v = fmaf(wgt, s.part_o[((int64_t)(base + i) * H + h) * L + c], v);
+  const float* part = s.part_o + ((int64_t)base * H + h) * L;
+  const bool vec = (L % 4 == 0) && ((o_s0 | o_s1) % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(o_lat) % (4 * sizeof(T)) == 0);
+  if (vec) {
+    for (int c = lane * 4; c < L; c += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < np; ++i) {
+        const float li = lse_p[(int64_t)i * H];
+        const float wi = li == -CUDART_INF_F ? 0.f : __expf(li - m);
+        const float4 v = *reinterpret_cast<const float4*>(part + i * pstride + c);
+        acc.x = fmaf(wi, v.x, acc.x);
+        acc.y = fmaf(wi, v.y, acc.y);
+        acc.z = fmaf(wi, v.z, acc.z);
+        acc.w = fmaf(wi, v.w, acc.w);
+      }
+      store4<T>(o + c, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
-    st(o + c, v * inv);
+  } else {
+    for (int c = lane; c < L; c += 32) {
+      float acc = 0.f;
+      for (int i = 0; i < np; ++i) {
+        const float li = lse_p[(int64_t)i * H];
+        const float wi = li == -CUDART_INF_F ? 0.f : __expf(li - m);
+        acc = fmaf(wi, part[i * pstride + c], acc);
+      }
+      st(o + c, acc * inv);
+    }
   }
-  if (threadIdx.x == 0 && lse_out)
-    lse_out[(int64_t)b * H + h] = tot > 0.f ? m + logf(tot) : -CUDART_INF_F;
+  if (lane == 0 && lse_out) lse_out[(int64_t)b * H + h] = tot > 0.f ? m + logf(tot) : -CUDART_INF_F;
 }
 
 // Causal prefill: one CTA per (query row, head group), no split.
@@ -425,7 +462,7 @@ cudaError_t launch_decode_combine(mla_dtype dt, const View3& o_lat, float* lse,
                                   const int32_t* seq_lens, int32_t B, int32_t H, int32_t L,
                                   const DecodeSched& s, cudaStream_t st) {
   (void)seq_lens;
-  const dim3 grid(B, H);
+  const dim3 grid(B, (H + 3) / 4);
   if (dt == MLA_F32)
     decode_combine_kernel<float><<<grid, 128, 0, st>>>((float*)o_lat.data, o_lat.s0, o_lat.s1, lse,
                                                        B, H, L, s);

@@ -6,8 +6,8 @@
 // M dimension of every MMA; keys come in tiles of 64 cache rows. The output
 // accumulator O is 128 x 512 fp32, which alone would fill a CTA's 512 TMEM
 // columns, so a cluster of two CTAs shares each row tile:
-//   CTA 0 owns latent columns   0..255
-//   CTA 1 owns latent columns 256..511 and the 64 rope columns
+//   CTA 0 owns latent columns   0..255 and rope columns 512..543
+//   CTA 1 owns latent columns 256..511 and rope columns 544..575
 // Each CTA TMA-loads only its columns of every cache row (a row crosses HBM
 // once per pair), computes its partial scores S_r = Q_r K_r^T, and the pair
 // swaps partials so both hold S = S_0 + S_1 (summed in the same order) and run
@@ -16,10 +16,12 @@
 //
 // Memory plan per CTA. Tensor memory holds everything the MMAs reuse:
 //   O half [0,256) fp32 | S [256,320) fp32 | P [320,352) bf16 pairs |
-//   Q half [352, 352 + 128 or 160) bf16 pairs,
+//   Q half [352, 480) latent, [480, 496) rope, bf16 pairs,
 // so both MMAs take their A operand from TMEM and shared memory only streams
-// the B operand (the cache tile). Shared memory holds 3 (rope) or 4 (NoPE)
-// cache-tile stages and two outgoing and two incoming exchange slots.
+// the B operand (the cache tile). The latent columns arrive in 64-column boxes
+// with 128-byte swizzle, the 32 rope columns in one box with 64-byte swizzle.
+// Shared memory holds 4 cache-tile stages (36 KB with rope, 32 KB without)
+// and two outgoing and two incoming exchange slots.
 //
 // Exchange. The SM-to-SM network moves only about 10 bytes per clock each way,
 // so the pair does not swap fp32 partial scores (32 KB per tile) but
@@ -68,6 +70,8 @@ __device__ unsigned g_tc_err = 0;
 constexpr int kRows = 128;                // M: query rows per tile
 constexpr int kKeysT = 64;                // keys per tile
 constexpr int kBoxBytesK = kKeysT * 128;  // one 64-column box of a key tile (8 KB)
+constexpr int kRopeHalf = 32;             // rope columns per CTA
+constexpr int kRopeBoxBytes = kKeysT * kRopeHalf * 2;   // 4 KB
 constexpr int kESlotBytes = kRows * kKeysT * 2;   // E = 2^(s - c) of one tile, bf16 (16 KB)
 constexpr int kXSlot = kESlotBytes + kRows * 4;     // + the rows' maxima c (16.5 KB)
 constexpr int kThreads = 384;
@@ -84,9 +88,8 @@ constexpr uint32_t kTmemQ = 352;
 
 template <int kRope>
 struct Cfg {
-  static constexpr int kBoxes = 4 + kRope / 64;      // boxes per CTA (max over the pair)
-  static constexpr int kStages = kRope ? 3 : 4;
-  static constexpr int kStageBytes = kBoxes * kBoxBytesK;
+  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = 4 * kBoxBytesK + (kRope ? kRopeBoxBytes : 0);
   static constexpr int kOffKV = 0;
   static constexpr int kOffXloc = kOffKV + kStages * kStageBytes;   // own E + c, 2 slots
   static constexpr int kOffXrem = kOffXloc + 2 * kXSlot;            // the peer's, 2 slots
@@ -251,7 +254,8 @@ __device__ __forceinline__ void set_abort(Bars& bars, uint32_t peer) {
 
 template <int kRope>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_attn_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const TcParams p) {
+    mla_attn_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap ropemap,
+                       const TcParams p) {
   using C = Cfg<kRope>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -264,9 +268,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int unit = (int)cluster_id_x(), nunits = (int)nclusters_x();
-  // columns of this CTA: latent [256*rank, +256) and, on rank 1, the rope
-  const int nbox = rank == 0 ? 4 : 4 + kRope / 64;
-  const int col0 = rank == 0 ? 0 : 256;
+  // columns of this CTA: latent [col0, col0 + 256) and rope [rope0, rope0 + 32)
+  const int col0 = 256 * (int)rank;
+  const int rope0 = p.L + kRopeHalf * (int)rank;
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -298,7 +302,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&kvmap);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kvmap);
+    if (kRope) tma_prefetch_desc(&ropemap);
+  }
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised before any remote access
   tc_fence_after();
@@ -352,15 +359,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   atomicOr(&g_tc_err, kErrDeviceData);
                   blks[i] = -1;
                 } else {
-                  bytes += (uint32_t)(nbox * rows_box * 128);
+                  bytes += (uint32_t)(rows_box * (4 * 128 + (kRope ? 2 * kRopeHalf : 0)));
                 }
               }
               mbar_arrive_expect_tx(&bars.kv_full[s], bytes);
               for (int i = 0; i < nsub; ++i) {
                 if (blks[i] < 0) continue;
-                for (int c = 0; c < nbox; ++c)
+                for (int c = 0; c < 4; ++c)
                   tma_load_3d(dst + c * kBoxBytesK + i * rows_box * 128, &kvmap, &bars.kv_full[s],
                               col0 + 64 * c, rows0[i], blks[i]);
+                if (kRope)
+                  tma_load_3d(dst + 4 * kBoxBytesK + i * rows_box * 2 * kRopeHalf, &ropemap, &bars.kv_full[s],
+                              rope0, rows0[i], blks[i]);
               }
               ++issued[s];
             }
@@ -403,10 +413,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               MLA_TRACE_AT(1, t);
               tc_fence_after();
               const uint32_t kb = kv_base + s * C::kStageBytes;
-              for (int c = 0; c < nbox; ++c)
+              for (int c = 0; c < 4; ++c)
                 for (int kk = 0; kk < 4; ++kk)
                   umma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + c * 32 + kk * 8,
                                sdesc_sw128(kb + c * kBoxBytesK + kk * 32, 16, 1024), id_qk, (c | kk) ? 1u : 0u);
+              if (kRope)
+                for (int kk = 0; kk < 2; ++kk)
+                  umma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + 128 + kk * 8,
+                               sdesc_sw64(kb + 4 * kBoxBytesK + kk * 32, 16, 512), id_qk, 1u);
               umma_commit(&bars.s_full);
               ++qk;
               did = true;
@@ -495,13 +509,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       {
-        const __nv_bfloat16* qrow = p.q + (int64_t)(sg.tok0 + t_in_tile) * p.q_s0 + (int64_t)head * p.q_s1 + col0;
-        for (int c = 0; c < nbox; ++c) {
+        const __nv_bfloat16* qrow = p.q + (int64_t)(sg.tok0 + t_in_tile) * p.q_s0 + (int64_t)head * p.q_s1;
+        for (int c = 0; c < 4 + (kRope ? 1 : 0); ++c) {
+          // latent chunk c: 64 values; chunk 4: this CTA's 32 rope values (upper columns zero)
+          const __nv_bfloat16* src = c < 4 ? qrow + col0 + c * 64 : qrow + rope0;
+          const int chunks = c < 4 ? 8 : 4;
           uint32_t v[32];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_valid) w = *reinterpret_cast<const uint4*>(qrow + c * 64 + i * 8);
+            if (row_valid && i < chunks) w = *reinterpret_cast<const uint4*>(src + i * 8);
             v[4 * i] = w.x;
             v[4 * i + 1] = w.y;
             v[4 * i + 2] = w.z;
@@ -782,7 +799,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
-                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {d0, d1, d2};
@@ -790,7 +807,7 @@ bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -826,12 +843,13 @@ int max_clusters() {
 }
 
 template <int kRope>
-cudaError_t launch_tc(const TcParams& p, const CUtensorMap& km, int clusters, cudaStream_t st) {
+cudaError_t launch_tc(const TcParams& p, const CUtensorMap& km, const CUtensorMap& rm, int clusters,
+                      cudaStream_t st) {
   using C = Cfg<kRope>;
   cudaError_t e = cudaFuncSetAttribute(mla_attn_tc_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  mla_attn_tc_kernel<kRope><<<dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st>>>(km, p);
+  mla_attn_tc_kernel<kRope><<<dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st>>>(km, rm, p);
   return cudaGetLastError();
 }
 
@@ -858,15 +876,21 @@ int tc_decode_units(int num_splits) {
 
 static cudaError_t run_tc(mla_dtype, TcParams& p, const View3& q, const CacheView& cv, int clusters,
                           cudaStream_t st) {
-  CUtensorMap km;
+  CUtensorMap km, rm;
   const int E = p.L + p.R;
+  const uint32_t rows_box = cv.page < 64 ? cv.page : 64;
   p.q = static_cast<const __nv_bfloat16*>(q.data);
   p.q_s0 = q.s0;
   p.q_s1 = q.s1;
+  // latent boxes: 64 columns x rows_box rows, 128-byte swizzle; rope boxes: 32 columns, 64-byte swizzle
   if (!make_map3d(&km, cv.data, E, cv.page, cv.num_blocks, (uint64_t)cv.s_row * 2, (uint64_t)cv.s_blk * 2, 64,
-                  cv.page < 64 ? cv.page : 64, 1))
+                  rows_box, 1, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  return p.R == 64 ? launch_tc<64>(p, km, clusters, st) : launch_tc<0>(p, km, clusters, st);
+  if (p.R == 0) return launch_tc<0>(p, km, km, clusters, st);
+  if (!make_map3d(&rm, cv.data, E, cv.page, cv.num_blocks, (uint64_t)cv.s_row * 2, (uint64_t)cv.s_blk * 2,
+                  kRopeHalf, rows_box, 1, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  return launch_tc<64>(p, km, rm, clusters, st);
 }
 
 cudaError_t launch_decode_tc(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,

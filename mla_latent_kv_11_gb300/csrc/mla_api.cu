@@ -152,6 +152,12 @@ int device_sm_count() {
   return cache[dev];
 }
 
+// bmm on the tensor cores when the shape and layout allow, else on CUDA cores.
+static cudaError_t launch_bmm(mla_dtype dt, const View3& out, const View3& a, const View3& b, cudaStream_t st) {
+  if (bmm_tc_supported(dt, out, a, b)) return launch_bmm_tc(out, a, b, st);
+  return launch_bmm_simt(dt, out, a, b, st);
+}
+
 // Work units of the split-KV decode: explicit, or two per SM.
 static int32_t decode_units(int32_t num_splits) {
   if (num_splits > 0) return num_splits;
@@ -186,8 +192,8 @@ mla_status mla_absorb_q(mla_dtype dtype, mla_tensor q_lat_out, mla_tensor q_nope
   MLA_TRY(check_dtype(dtype));
   MLA_TRY(check_bmm(q_lat_out, q_nope, w_uk, "q_lat_out", "q_nope", "w_uk"));
   if (numel(q_lat_out) == 0) return MLA_OK;
-  return cuda_status(launch_bmm_simt(dtype, view3(q_lat_out), view3(q_nope), view3(w_uk),
-                                     (cudaStream_t)stream), "mla_absorb_q");
+  return cuda_status(launch_bmm(dtype, view3(q_lat_out), view3(q_nope), view3(w_uk), (cudaStream_t)stream),
+                     "mla_absorb_q");
 }
 
 mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tensor w_uv,
@@ -196,8 +202,8 @@ mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tenso
   MLA_TRY(check_dtype(dtype));
   MLA_TRY(check_bmm(out, o_lat, w_uv, "out", "o_lat", "w_uv"));
   if (numel(out) == 0) return MLA_OK;
-  return cuda_status(launch_bmm_simt(dtype, view3(out), view3(o_lat), view3(w_uv),
-                                     (cudaStream_t)stream), "mla_v_up");
+  return cuda_status(launch_bmm(dtype, view3(out), view3(o_lat), view3(w_uv), (cudaStream_t)stream),
+                     "mla_v_up");
 }
 
 mla_status mla_concat_q(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope, mla_tensor rope,
@@ -366,7 +372,8 @@ mla_status mla_device_error(void* stream) {
   g_msg[0] = 0;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "mla_device_error: stream synchronize");
-  unsigned bits = copy_errors_read_clear() | attn_simt_errors_read_clear() | attn_tc_errors_read_clear();
+  unsigned bits = copy_errors_read_clear() | attn_simt_errors_read_clear() | attn_tc_errors_read_clear() |
+                  bmm_tc_errors_read_clear();
   if (bits & kErrTimeout) return fail(MLA_ERR_TIMEOUT, "a bounded device-side wait gave up");
   if (bits & kErrDeviceData)
     return fail(MLA_ERR_DEVICE_DATA, "a slot, block id or sequence length was out of range");

@@ -65,6 +65,9 @@ cudaError_t launch_cache_write(mla_dtype dt, const View3& cache, const View3& kv
                                int64_t T, cudaStream_t st);
 cudaError_t launch_bmm_simt(mla_dtype dt, const View3& out, const View3& a, const View3& b,
                             cudaStream_t st);
+// Tensor-core bmm (bmm_tc.cu): bf16, K % 64 == 0, N % 128 == 0, 16-byte aligned views.
+bool bmm_tc_supported(mla_dtype dt, const View3& out, const View3& a, const View3& b);
+cudaError_t launch_bmm_tc(const View3& out, const View3& a, const View3& b, cudaStream_t st);
 
 cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
                                    int32_t page, const DecodeSched& s, cudaStream_t st);
@@ -104,5 +107,6 @@ mla_status report_status(mla_status st, const char* fmt, ...);
 unsigned copy_errors_read_clear();
 unsigned attn_simt_errors_read_clear();
 unsigned attn_tc_errors_read_clear();
+unsigned bmm_tc_errors_read_clear();
 
 }  // namespace mla
