@@ -37,13 +37,16 @@
 // two halves concurrently.
 //
 // Roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs (a polling
-// state machine that issues whichever of QK(g+1) and PV(g) is ready), warp 2
+// state machine that issues whichever of QK(g+1) and PV(g) is ready; the warp
+// runs it converged and an elected lane issues, which keeps the N=64 QK MMAs at
+// the tensor core's rate instead of the issue rate of one thread), warp 2
 // owns the TMEM allocation, warps 4..7 load Q into TMEM and run the exchange,
 // warps 8..11 run the softmax, the O rescale and the epilogue, one thread per
 // query row (TMEM lane) in each group; warp 3 forwards the softmax group's
 // "incoming buffer read" signals to the peer (a cluster-scope release stalls
-// the issuing thread for about a microsecond, so it is kept off the softmax). Every wait is bounded in time; a
-// timeout winds the kernel down and reports MLA_ERR_TIMEOUT instead of hanging.
+// the issuing thread for about a microsecond, so it is kept off the softmax).
+// Every wait is bounded in time; a timeout winds the kernel down and reports
+// MLA_ERR_TIMEOUT instead of hanging.
 //
 // The running reference maximum is updated lazily (O and the denominator are
 // rescaled only when the bound c_0 + c_1 grows by more than 2^8, so P stays
@@ -257,6 +260,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_attn_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap ropemap,
                        const TcParams p) {
   using C = Cfg<kRope>;
+  static_assert(sizeof(Bars) <= C::kBarBytes, "barrier block overflows its slot");
+  static_assert(C::kSmemAlloc <= 232448, "shared memory beyond the 227 KB a CTA may hold");
+  static_assert(C::kStages <= 4, "kv barrier arrays hold 4 stages");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
@@ -388,80 +394,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (issued[s] > 0) mbar_wait(&bars.kv_full[s], (issued[s] - 1) & 1, &dummy);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      Walker wk;
-      wk.init(p, unit, nunits);
-      Seg sg;
-      int gt = 0, seg_i = 0;
-      bool ok = true;
-      const uint32_t id_qk = idesc_bf16(kRows, kKeysT, false, false);
-      const uint32_t id_pv = idesc_bf16(kRows, 256, false, true);
-      const uint32_t kv_base = smem_u32(sKV);
-      while (ok && wk.next(p, sg)) {
-        const int nt = ntiles(sg);
-        ok = mbar_wait(&bars.q_ready, seg_i & 1, abort);
-        int qk = 0, pv = 0;
-        uint64_t last = globaltimer_ns();
-        uint32_t spins = 0;
-        while (ok && pv < nt) {
-          bool did = false;
-          if (qk < nt) {
-            const int t = gt + qk, s = t % C::kStages;
-            // S is single-buffered: QK(t) needs S(t-1) read out by the softmax group
-            if (mbar_poll(&bars.kv_full[s], (t / C::kStages) & 1) && mbar_poll(&bars.s_empty, (t & 1) ^ 1)) {
-              MLA_TRACE_AT(1, t);
-              tc_fence_after();
-              const uint32_t kb = kv_base + s * C::kStageBytes;
-              for (int c = 0; c < 4; ++c)
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + c * 32 + kk * 8,
-                               sdesc_sw128(kb + c * kBoxBytesK + kk * 32, 16, 1024), id_qk, (c | kk) ? 1u : 0u);
-              if (kRope)
-                for (int kk = 0; kk < 2; ++kk)
-                  umma_bf16_ta(tmem + kTmemS, tmem + kTmemQ + 128 + kk * 8,
-                               sdesc_sw64(kb + 4 * kBoxBytesK + kk * 32, 16, 512), id_qk, 1u);
-              umma_commit(&bars.s_full);
-              ++qk;
-              did = true;
-            }
-          }
-          if (pv < qk) {
-            const int t = gt + pv, s = t % C::kStages;
-            const bool o_free = pv > 0 || seg_i == 0 || mbar_poll(&bars.o_empty, (seg_i - 1) & 1);
-            if (o_free && mbar_poll(&bars.p_full, t & 1)) {
-              MLA_TRACE_AT(2, t);
-              tc_fence_after();
-              const uint32_t vb = kv_base + s * C::kStageBytes;
+    // ------------------------------------------------------------ MMA issuer. The whole
+    // warp walks the state machine in lockstep (every decision is lane 0's, broadcast) and
+    // one elected lane issues each MMA and commit.
+    auto uni = [&](bool v) { return __shfl_sync(0xffffffffu, v ? 1 : 0, 0) != 0; };
+    Walker wk;
+    wk.init(p, unit, nunits);
+    Seg sg;
+    int gt = 0, seg_i = 0;
+    bool ok = true;
+    constexpr uint32_t id_qk = idesc_bf16(kRows, kKeysT, false, false);
+    constexpr uint32_t id_pv = idesc_bf16(kRows, 256, false, true);
+    const uint32_t kv_base = smem_u32(sKV);
+    while (ok && wk.next(p, sg)) {
+      const int nt = ntiles(sg);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_ready, seg_i & 1, abort));
+      int qk = 0, pv = 0;
+      uint64_t last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (ok && pv < nt) {
+        bool did = false;
+        if (qk < nt) {
+          const int t = gt + qk, s = t % C::kStages;
+          // S is single-buffered: QK(t) needs S(t-1) read out by the exchange group
+          if (uni(mbar_poll(&bars.kv_full[s], (t / C::kStages) & 1) && mbar_poll(&bars.s_empty, (t & 1) ^ 1))) {
+            MLA_TRACE_AT(1, t);
+            tc_fence_after();
+            const uint32_t kb = kv_base + s * C::kStageBytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_bf16_ta(tmem + kTmemO, tmem + kTmemP + kk * 8, sdesc_sw128(vb + kk * 16 * 128, kBoxBytesK, 1024),
-                             id_pv, (pv > 0 || kk > 0) ? 1u : 0u);
-              umma_commit(&bars.kv_empty[s]);
-              umma_commit(&bars.pv_done);
-              if (pv == nt - 1) umma_commit(&bars.seg_done);
-              ++pv;
-              did = true;
+                umma_bf16_ta_elect(tmem + kTmemS, tmem + kTmemQ + c * 32 + kk * 8,
+                                   sdesc_sw128(kb + c * kBoxBytesK + kk * 32, 16, 1024), id_qk, (c | kk) ? 1u : 0u);
+            if (kRope) {
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk)
+                umma_bf16_ta_elect(tmem + kTmemS, tmem + kTmemQ + 128 + kk * 8,
+                                   sdesc_sw64(kb + 4 * kBoxBytesK + kk * 32, 16, 512), id_qk, 1u);
             }
-          }
-          if (did) {
-            spins = 0;
-            last = globaltimer_ns();
-          } else {
-            __nanosleep(32);   // leave the issue slots to the softmax warps
-            if ((++spins & 255u) == 0 && (*abort || globaltimer_ns() - last > kWaitLimitNs)) ok = false;
+            umma_commit_elect(&bars.s_full);
+            ++qk;
+            did = true;
           }
         }
-        if (!ok) break;
-        if (nt == 0) umma_commit(&bars.seg_done);
-        gt += nt;
-        ++seg_i;
+        if (pv < qk) {
+          const int t = gt + pv, s = t % C::kStages;
+          const bool o_free = pv > 0 || seg_i == 0 || mbar_poll(&bars.o_empty, (seg_i - 1) & 1);
+          if (uni(o_free && mbar_poll(&bars.p_full, t & 1))) {
+            MLA_TRACE_AT(2, t);
+            tc_fence_after();
+            const uint32_t vb = kv_base + s * C::kStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ta_elect(tmem + kTmemO, tmem + kTmemP + kk * 8,
+                                 sdesc_sw128(vb + kk * 16 * 128, kBoxBytesK, 1024), id_pv, (pv > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elect(&bars.kv_empty[s]);
+            umma_commit_elect(&bars.pv_done);
+            if (pv == nt - 1) umma_commit_elect(&bars.seg_done);
+            ++pv;
+            did = true;
+          }
+        }
+        if (did) {
+          spins = 0;
+          last = globaltimer_ns();
+        } else {
+          __nanosleep(32);   // leave the issue slots to the softmax warps
+          if ((++spins & 255u) == 0 && (*abort || globaltimer_ns() - last > kWaitLimitNs)) ok = false;
+          ok = uni(ok);
+        }
       }
-      if (!ok) set_abort(bars, peer);
-      // every MMA this thread issued is complete before the TMEM is released
-      umma_commit(&bars.mma_final);
-      volatile int dummy = 0;
-      mbar_wait(&bars.mma_final, 0, &dummy);
+      if (!ok) break;
+      if (nt == 0) umma_commit_elect(&bars.seg_done);
+      gt += nt;
+      ++seg_i;
     }
+    if (!ok && lane == 0) set_abort(bars, peer);
+    __syncwarp();
+    // every MMA this warp issued is complete before the TMEM is released
+    umma_commit_elect(&bars.mma_final);
+    volatile int dummy = 0;
+    mbar_wait(&bars.mma_final, 0, &dummy);
+    __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ forwarder: releases the
     // incoming buffers to the peer once the softmax group has read them

@@ -7,7 +7,7 @@
 // their strided views (the usual transposed [H,B,P] operand and [H,B,L]
 // output cost nothing extra): A tiles are K-major [128 rows x 64 k] boxes,
 // B tiles are [64 k x 64 n] boxes used as an MN-major operand. A 4-stage ring
-// of k-steps feeds one issuing thread; the fp32 accumulator sits in TMEM. The
+// of k-steps feeds one issuing warp; the fp32 accumulator sits in TMEM. The
 // epilogue converts to bf16 through a 128-byte-swizzled staging tile and
 // writes it with TMA stores, which clip rows past M (the decode batch, padded
 // to 128 rows by the loads' zero fill).
@@ -102,22 +102,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int dummy = 0;
     for (int s = 0; s < kStages; ++s)
       if (issued[s] > 0) mbar_wait(&full[s], (issued[s] - 1) & 1, &dummy);
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer
-    const uint32_t idesc = idesc_bf16(kBM, kBN, false, true);
+  } else if (warp == 1) {
+    // MMA issuer: the converged warp walks the k-steps, one elected lane issues
+    constexpr uint32_t idesc = idesc_bf16(kBM, kBN, false, true);
     bool ok = true;
     for (int ks = 0; ks < ksteps && ok; ++ks) {
       const int s = ks % kStages;
-      ok = mbar_wait(&full[s], (ks / kStages) & 1, abort);
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (ks / kStages) & 1, abort));
       if (!ok) break;
       tc_fence_after();
       const uint32_t a = smem_u32(smem + s * C::kStageBytes), b = a + kABytes;
+#pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk)
-        umma_bf16(tmem, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 16 * 128, kBBox, 1024), idesc,
-                  (ks | kk) ? 1u : 0u);
-      umma_commit(&empty[s]);
+        umma_bf16_elect(tmem, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 16 * 128, kBBox, 1024), idesc,
+                        (ks | kk) ? 1u : 0u);
+      umma_commit_elect(&empty[s]);
     }
-    umma_commit(done);
+    umma_commit_elect(done);
     volatile int dummy = 0;
     mbar_wait(done, 0, &dummy);
   }
