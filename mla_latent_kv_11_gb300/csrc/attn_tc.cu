@@ -492,6 +492,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int t = gt + j, b = t & 1;
           ok = mbar_wait(&bars.xin_free[b], (t >> 1) & 1, abort);
           if (ok) mbar_arrive_remote(&bars.x_empty[b], peer);
+#ifdef MLA_TRACE
+          if (unit == 0 && t < 512) g_trace2[rank][4][t] = clock64();
+#endif
         }
         gt += nt;
       }
@@ -602,6 +605,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (row == 0) {
           // the peer's incoming slot b is free once it has consumed tile t - 2
           sent = mbar_wait<true>(&bars.x_empty[b], ((t >> 1) & 1) ^ 1, abort);
+          MLA_TRACE2_AT(0, t);
           if (sent) {
             bulk_copy_to_peer(peer_rem0 + b * kXSlot, slot, kXSlot, peer_xfull0 + b * 8);
             bulk_commit_group();
@@ -632,8 +636,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m = -CUDART_INF_F, l = 0.f;    // running reference max (base 2) and denominator
       for (int j = 0; ok && j < nt; ++j) {
         const int g = gt + j, b = g & 1;
-        ok = group_all(mbar_wait(&bars.own_ready[b], (g >> 1) & 1, abort) &&
-                       mbar_wait<true>(&bars.x_full[b], (g >> 1) & 1, abort));
+        MLA_TRACE2_AT(1, g);
+        const bool own_ok = mbar_wait(&bars.own_ready[b], (g >> 1) & 1, abort);
+        MLA_TRACE2_AT(2, g);
+        ok = group_all(own_ok && mbar_wait<true>(&bars.x_full[b], (g >> 1) & 1, abort));
+        MLA_TRACE2_AT(3, g);
         if (!ok) break;
         const unsigned char* own = sXloc + b * kXSlot;
         const unsigned char* rem = sXrem + b * kXSlot;
