@@ -16,7 +16,10 @@
 //
 // Memory plan per CTA. Tensor memory holds everything the MMAs reuse:
 //   O half [0,256) fp32 | S [256,320) fp32 | P [320,352) bf16 pairs |
-//   Q half [352, 480) latent, [480, 496) rope, bf16 pairs,
+//   Q half [352, 480) latent, [480, 496) rope, bf16 pairs | l [496,512) fp32,
+// where l, the row sums of P, comes from an N=16 MMA of P against a tile of
+// ones issued with each PV (so the denominator sums exactly the bf16 P that O
+// accumulates, and the softmax warps never add P up),
 // so both MMAs take their A operand from TMEM and shared memory only streams
 // the B operand (the cache tile). The latent columns arrive in 64-column boxes
 // with 128-byte swizzle, the 32 rope columns in one box with 64-byte swizzle.
@@ -25,12 +28,14 @@
 //
 // Exchange. The SM-to-SM network moves only about 10 bytes per clock each way,
 // so the pair does not swap fp32 partial scores (32 KB per tile) but
-// exponentials: each CTA takes its row maximum c_r of x_r = s_r * scale * log2 e
-// and sends E_r = 2^(x_r - c_r) in bf16 with c_r (16.5 KB per tile). Since
+// exponentials: each CTA takes its row maximum of x_r = s_r * scale * log2 e,
+// rounded up to an integer c_r, and sends E_r = 2^(x_r - c_r) in bf16 with c_r
+// (16.5 KB per tile). Since
 //   2^(x_0 + x_1 - m) = E_0 * E_1 * 2^(c_0 + c_1 - m),
 // both CTAs form the same P from the same bf16 operands in the same order;
 // c_0 + c_1 bounds the row maximum from above, so nothing can overflow, and
-// the extra rounding is that of the bf16 P the PV MMA takes anyway. A
+// it is an integer, so every rescaling factor is an exact power of two: P is
+// E_0 * E_1 rounded once to bf16 (the PV MMA takes bf16 anyway). A
 // dedicated exchange warpgroup reads S out of TMEM as soon as the MMA has
 // produced it, computes c and E and pushes them with one bulk copy (completion
 // counted in bytes on the peer's barrier); the softmax warpgroup combines the
@@ -48,9 +53,10 @@
 // Every wait is bounded in time; a timeout winds the kernel down and reports
 // MLA_ERR_TIMEOUT instead of hanging.
 //
-// The running reference maximum is updated lazily (O and the denominator are
-// rescaled only when the bound c_0 + c_1 grows by more than 2^8, so P stays
-// below 256). P is rounded to bf16 for the PV MMA.
+
+// The running reference maximum m is updated lazily: O and its denominator are
+// rescaled only when the bound c_0 + c_1 exceeds m by more than 8, so P stays
+// below 2^8.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -88,13 +94,16 @@ constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;
 constexpr uint32_t kTmemP = 320;
 constexpr uint32_t kTmemQ = 352;
+constexpr uint32_t kTmemL = 496;          // row sums of P, accumulated by the tensor core (16 equal columns)
+constexpr int kOnesBytes = 16 * kKeysT * 2;   // a 16 x 64 tile of bf16 ones: B operand of the row-sum MMA
 
 template <int kRope>
 struct Cfg {
   static constexpr int kStages = 4;
   static constexpr int kStageBytes = 4 * kBoxBytesK + (kRope ? kRopeBoxBytes : 0);
   static constexpr int kOffKV = 0;
-  static constexpr int kOffXloc = kOffKV + kStages * kStageBytes;   // own E + c, 2 slots
+  static constexpr int kOffOnes = kOffKV + kStages * kStageBytes;   // 1 KB aligned: stages are
+  static constexpr int kOffXloc = kOffOnes + kOnesBytes;            // own E + c, 2 slots
   static constexpr int kOffXrem = kOffXloc + 2 * kXSlot;            // the peer's, 2 slots
   static constexpr int kOffBar = (kOffXrem + 2 * kXSlot + 127) & ~127;
   static constexpr int kBarBytes = 1024;
@@ -246,6 +255,11 @@ struct Walker {
   }
 };
 
+// 2^d for an integer-valued d <= 127, exactly (built from the exponent bits); 0 below -126.
+__device__ __forceinline__ float exp2_int(float d) {
+  return d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
+}
+
 __device__ __forceinline__ int ntiles(const Seg& s) { return (s.k1 - s.k0 + kKeysT - 1) / kKeysT; }
 
 __device__ __forceinline__ void set_abort(Bars& bars, uint32_t peer) {
@@ -312,6 +326,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&kvmap);
     if (kRope) tma_prefetch_desc(&ropemap);
   }
+  for (int i = tid; i < kOnesBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + C::kOffOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  fence_proxy_async_smem();   // the ones tile is read by the tensor core (async proxy)
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised before any remote access
   tc_fence_after();
@@ -405,7 +422,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     constexpr uint32_t id_qk = idesc_bf16(kRows, kKeysT, false, false);
     constexpr uint32_t id_pv = idesc_bf16(kRows, 256, false, true);
+    constexpr uint32_t id_sum = idesc_bf16(kRows, 16, false, false);
     const uint32_t kv_base = smem_u32(sKV);
+    const uint32_t ones_base = smem_u32(smem + C::kOffOnes);
     while (ok && wk.next(p, sg)) {
       const int nt = ntiles(sg);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_ready, seg_i & 1, abort));
@@ -449,6 +468,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16_ta_elect(tmem + kTmemO, tmem + kTmemP + kk * 8,
                                  sdesc_sw128(vb + kk * 16 * 128, kBoxBytesK, 1024), id_pv, (pv > 0 || kk > 0) ? 1u : 0u);
+            // l += P * ones: the row sums of exactly the bf16 P that O accumulates
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ta_elect(tmem + kTmemL, tmem + kTmemP + kk * 8, sdesc_sw128(ones_base + kk * 32, 16, 1024),
+                                 id_sum, (pv > 0 || kk > 0) ? 1u : 0u);
             umma_commit_elect(&bars.kv_empty[s]);
             umma_commit_elect(&bars.pv_done);
             if (pv == nt - 1) umma_commit_elect(&bars.seg_done);
@@ -576,7 +600,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             c = fmaxf(c, sv[k]);
           }
         }
-        c = c == -CUDART_INF_F ? -CUDART_INF_F : c * p.scale_log2;
+        // rounded up to an integer: still an upper bound, and it makes every factor
+        // 2^(M - m) of the softmax an exact power of two
+        c = c == -CUDART_INF_F ? -CUDART_INF_F : ceilf(c * p.scale_log2);
         const float neg_c = c == -CUDART_INF_F ? 0.f : -c;
         uint32_t ek[32];
 #pragma unroll
@@ -633,7 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (ok && wk.next(p, sg)) {
       const int nt = ntiles(sg);
       const bool row_valid = row < p.H * p.tpt && t_in_tile < sg.ntok;
-      float m = -CUDART_INF_F, l = 0.f;    // running reference max (base 2) and denominator
+      float m = -CUDART_INF_F;             // running reference max (base 2); the denominator is in TMEM
       for (int j = 0; ok && j < nt; ++j) {
         const int g = gt + j, b = g & 1;
         MLA_TRACE2_AT(1, g);
@@ -660,32 +686,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars.xin_free[b]);
           mbar_arrive(&bars.xloc_free[b]);
         }
-        // ---- tile upper bound M = c_0 + c_1 (same order in both CTAs); lazy reference max
-        const float c0 = rank == 0 ? c_own : c_rem, c1 = rank == 0 ? c_rem : c_own;
-        const float M = (c0 == -CUDART_INF_F || c1 == -CUDART_INF_F) ? -CUDART_INF_F : c0 + c1;
+        MLA_TRACE2_AT(5, g);
+        // ---- tile upper bound M = c_0 + c_1; IEEE addition and multiplication commute, so
+        // own-then-peer operands give both CTAs bit-identical M and P without knowing rank
+        const float M = (c_own == -CUDART_INF_F || c_rem == -CUDART_INF_F) ? -CUDART_INF_F : c_own + c_rem;
         float alpha = 1.f;
         bool rescale_o = false;
         if (M > m + kLazyRescale || (m == -CUDART_INF_F && M > -CUDART_INF_F)) {
-          alpha = m == -CUDART_INF_F ? 0.f : ex2_approx(m - M);
+          alpha = m == -CUDART_INF_F ? 0.f : exp2_int(m - M);
           rescale_o = (m != -CUDART_INF_F) && j > 0;
           m = M;
         }
-        const float factor = M == -CUDART_INF_F ? 0.f : ex2_approx(M - m);
-        // ---- P = E_0 * E_1 * 2^(M - m): identical operands and order in both CTAs
-        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(rank == 0 ? eo : er);
-        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(rank == 0 ? er : eo);
-        float sum = 0.f;
+        const float factor = M == -CUDART_INF_F ? 0.f : exp2_int(M - m);
+        MLA_TRACE2_AT(6, g);
+        // ---- P = (E_own * E_peer) * 2^(M - m): the same value in both CTAs
+        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(eo);
+        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(er);
+        // packed bf16 products: E_own * E_peer rounded once; the factor is an exact power of two
+        const __nv_bfloat162 f2 = __float2bfloat162_rn(factor);
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w0[k]));
-          const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1[k]));
-          const float p0 = (a0.x * a1.x) * factor, p1 = (a0.y * a1.y) * factor;
-          sum += p0 + p1;
-          const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-          pk[k] = *reinterpret_cast<const uint32_t*>(&h);
+          const __nv_bfloat162 e = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&w0[k]),
+                                           *reinterpret_cast<const __nv_bfloat162*>(&w1[k]));
+          const __nv_bfloat162 q = __hmul2(e, f2);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&q);
         }
-        l = l * alpha + sum;
         MLA_TRACE_AT(7, g);
         // ---- P(g) replaces P(g-1) in TMEM once PV(g-1) is done; O is rescaled then too
         if (g > 0) {
@@ -705,6 +731,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) v[i] *= f;
             tmem_st32(tmem + lane_addr + kTmemO + c, v);
           }
+          float lv[16];
+          tmem_ld16(tmem + lane_addr + kTmemL, lv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lv[i] *= f;
+          tmem_st16(tmem + lane_addr + kTmemL, lv);
         }
         tmem_st32u(tmem + lane_addr + kTmemP, pk);
         // rows of a partial tile past the sequence: zero their V so garbage cannot reach O
@@ -721,6 +753,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
         tmem_st_wait();
+        MLA_TRACE2_AT(7, g);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full);
@@ -731,6 +764,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = group_all(mbar_wait(&bars.seg_done, seg_i & 1, abort));
       if (!ok) break;
       tc_fence_after();
+      float l = 0.f;   // an empty segment issued no MMA: its sum columns hold stale data
+      if (nt > 0) {
+        float lv[16];
+        tmem_ld16(tmem + lane_addr + kTmemL, lv);
+        tmem_ld_wait();
+        l = lv[0];
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int tok = sg.tok0 + t_in_tile;
       for (int c = 0; c < 256; c += 32) {
