@@ -573,12 +573,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.q_ready);
       }
+      bool sent = true;   // row 0: its last push went out
       for (int j = 0; ok && j < nt; ++j) {
         const int t = gt + j, b = t & 1;
-        // ---- S(t) out of TMEM; the MMA may then compute S(t+1)
-        ok = group_all(mbar_wait(&bars.s_full, t & 1, abort));
+        // ---- one group decision per tile: S(t) is in TMEM, outgoing slot b is free (the
+        // softmax group has read tile t-2 from it, and the push of tile t-2 has left it: all
+        // pushes but the latest, tile t-1's, have been read) and row 0's last push went out
+        bool mine = mbar_wait(&bars.s_full, t & 1, abort) &&
+                    mbar_wait(&bars.xloc_free[b], ((t >> 1) & 1) ^ 1, abort);
+        if (row == 0) {
+          mine = mine && sent;
+          bulk_wait_read_but_last();
+        }
+        ok = group_all(mine);
         if (!ok) break;
         MLA_TRACE_AT(3, t);
+        // ---- S(t) out of TMEM; the MMA may then compute S(t+1)
         tc_fence_after();
         float sv[64];
         tmem_ld32(tmem + lane_addr + kTmemS, *reinterpret_cast<float(*)[32]>(sv));
@@ -589,17 +599,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars.s_empty);
         // ---- own row max c (base 2, scale folded in) and E = 2^(x - c) in bf16
         const int kbase = sg.k0 + j * kKeysT;
-        float c = -CUDART_INF_F;
-        if (__all_sync(0xffffffffu, kbase + kKeysT <= limit)) {
+        if (!__all_sync(0xffffffffu, kbase + kKeysT <= limit)) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) c = fmaxf(c, sv[k]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            sv[k] = kbase + k < limit ? sv[k] : -CUDART_INF_F;
-            c = fmaxf(c, sv[k]);
-          }
+          for (int k = 0; k < 64; ++k) sv[k] = kbase + k < limit ? sv[k] : -CUDART_INF_F;
         }
+        float mx[8];   // eight running maxima and a tree: no 64-long dependency chain
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+#pragma unroll
+        for (int k = 8; k < 64; ++k) mx[k & 7] = fmaxf(mx[k & 7], sv[k]);
+        float c = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         // rounded up to an integer: still an upper bound, and it makes every factor
         // 2^(M - m) of the softmax an exact power of two
         c = c == -CUDART_INF_F ? -CUDART_INF_F : ceilf(c * p.scale_log2);
@@ -611,11 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                          ex2_approx(fmaf(sv[k + 1], p.scale_log2, neg_c)));
           ek[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        // ---- into the outgoing slot b once the softmax group and the last push are done with it
-        ok = group_all(mbar_wait(&bars.xloc_free[b], ((t >> 1) & 1) ^ 1, abort));
-        if (!ok) break;
-        if (row == 0) bulk_wait_read_all();
-        named_bar(kXchgBar, 128);
+        // ---- into outgoing slot b, then to the peer once its incoming slot b is free
         unsigned char* slot = sXloc + b * kXSlot;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
@@ -627,7 +632,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         MLA_TRACE_AT(4, t);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.own_ready[b]);
-        bool sent = true;
         if (row == 0) {
           // the peer's incoming slot b is free once it has consumed tile t - 2
           sent = mbar_wait<true>(&bars.x_empty[b], ((t >> 1) & 1) ^ 1, abort);
@@ -637,8 +641,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bulk_commit_group();
           }
         }
-        ok = group_all(sent);
       }
+      if (!ok) break;
+      ok = group_all(sent);   // the segment's last push went out
       if (!ok) break;
       gt += nt;
       ++seg_i;
