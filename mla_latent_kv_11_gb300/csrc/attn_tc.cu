@@ -81,8 +81,10 @@ constexpr int kKeysT = 64;                // keys per tile
 constexpr int kBoxBytesK = kKeysT * 128;  // one 64-column box of a key tile (8 KB)
 constexpr int kRopeHalf = 32;             // rope columns per CTA
 constexpr int kRopeBoxBytes = kKeysT * kRopeHalf * 2;   // 4 KB
-constexpr int kESlotBytes = kRows * kKeysT * 2;   // E = 2^(s - c) of one tile, bf16 (16 KB)
-constexpr int kXSlot = kESlotBytes + kRows * 4;     // + the rows' maxima c (16.5 KB)
+constexpr int kHalfKeys = kKeysT / 2;             // keys per exchange piece
+constexpr int kESlotBytes = kRows * kHalfKeys * 2; // E = 2^(x - c) of half a tile, bf16 (8 KB)
+constexpr int kXSlot = kESlotBytes + kRows * 4;     // + the rows' maxima c (8.5 KB): one piece
+constexpr int kInSlots = 3;                         // incoming pieces: a ring of three
 constexpr int kThreads = 384;
 constexpr int kXchgWarp0 = 4;             // exchange warpgroup: warps 4..7
 constexpr int kSoftmaxWarp0 = 8;          // softmax warpgroup: warps 8..11
@@ -99,26 +101,30 @@ constexpr int kOnesBytes = 16 * kKeysT * 2;   // a 16 x 64 tile of bf16 ones: B 
 
 template <int kRope>
 struct Cfg {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 5;
   static constexpr int kStageBytes = 4 * kBoxBytesK + (kRope ? kRopeBoxBytes : 0);
   static constexpr int kOffKV = 0;
   static constexpr int kOffOnes = kOffKV + kStages * kStageBytes;   // 1 KB aligned: stages are
-  static constexpr int kOffXloc = kOffOnes + kOnesBytes;            // own E + c, 2 slots
-  static constexpr int kOffXrem = kOffXloc + 2 * kXSlot;            // the peer's, 2 slots
-  static constexpr int kOffBar = (kOffXrem + 2 * kXSlot + 127) & ~127;
-  static constexpr int kBarBytes = 1024;
+  static constexpr int kOffXloc = kOffOnes + kOnesBytes;            // own E + c of a tile: 2 pieces
+  static constexpr int kOffXrem = kOffXloc + 2 * kXSlot;            // the peer's pieces: a ring of 3
+  static constexpr int kOffBar = (kOffXrem + kInSlots * kXSlot + 127) & ~127;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmem = kOffBar + kBarBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;    // slack for 1 KB alignment
 };
 
 struct Bars {
-  uint64_t kv_full[4], kv_empty[4];
+  uint64_t kv_full[8], kv_empty[8];
   uint64_t s_full, s_empty, p_full, pv_done;
   uint64_t seg_done, o_empty, q_ready, mma_final;
-  uint64_t x_full[2], x_empty[2];
-  uint64_t own_ready[2]; // own E and c of the tile are in outgoing slot b
-  uint64_t xloc_free[2]; // the softmax group has read outgoing slot b
-  uint64_t xin_free[2];  // the softmax group has read incoming slot b
+  // Exchange. Half h of tile t (keys [32h, 32h + 32)) is piece q = 2t + h; the peer's
+  // piece q lands in incoming slot q % 3 (those barriers complete a phase every three
+  // pieces); the own tile sits in the outgoing slot (one phase per tile).
+  uint64_t own_ready;          // own E and c of the tile are in the outgoing slot
+  uint64_t xloc_free;          // the softmax group has read the outgoing slot
+  uint64_t x_full[kInSlots];   // the peer's piece has landed in incoming slot i
+  uint64_t x_empty[kInSlots];  // the peer has read its incoming slot i (arrived on by the peer)
+  uint64_t xin_free[kInSlots]; // the softmax group has read incoming slot i
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -127,6 +133,7 @@ struct Bars {
 // Cycle stamps of pipeline events of work unit 0, for tuning builds only.
 __device__ long long g_trace[2][8][512];
 __device__ long long g_trace2[2][8][512];
+__device__ long long g_cta_time[512][4];   // per CTA: SM id, start, end (globaltimer ns), tiles
 #define MLA_TRACE_AT(ev, g)                                              \
   do {                                                                    \
     if (unit == 0 && (g) < 512) g_trace[rank][ev][(g)] = clock64();      \
@@ -276,13 +283,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   using C = Cfg<kRope>;
   static_assert(sizeof(Bars) <= C::kBarBytes, "barrier block overflows its slot");
   static_assert(C::kSmemAlloc <= 232448, "shared memory beyond the 227 KB a CTA may hold");
-  static_assert(C::kStages <= 4, "kv barrier arrays hold 4 stages");
+  static_assert(C::kStages <= 8, "kv barrier arrays hold 8 stages");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + C::kOffBar);
   unsigned char* sKV = smem + C::kOffKV;
-  unsigned char* sXloc = smem + C::kOffXloc;   // [2] x (E [128 rows x 128 B, chunk-swizzled] | c [128])
+  unsigned char* sXloc = smem + C::kOffXloc;   // 2 pieces x (E [128 rows x 64 B, chunk-rotated] | c [128])
   unsigned char* sXrem = smem + C::kOffXrem;   // same layout, written by the peer
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -305,18 +312,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars.o_empty, 4);
     mbar_init(&bars.q_ready, 4);
     mbar_init(&bars.mma_final, 1);
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(&bars.own_ready, 4);
+    mbar_init(&bars.xloc_free, 1);
+    for (int i = 0; i < kInSlots; ++i) {
       mbar_init(&bars.x_full[i], 1);
       mbar_init(&bars.x_empty[i], 1);
-      mbar_init(&bars.own_ready[i], 4);
-      mbar_init(&bars.xloc_free[i], 1);
       mbar_init(&bars.xin_free[i], 1);
     }
     bars.abort_flag = 0;
     fence_mbar_init();
-    // the incoming buffers of tiles 0 and 1 are armed before the peer can send
-    mbar_arrive_expect_tx(&bars.x_full[0], kXSlot);
-    mbar_arrive_expect_tx(&bars.x_full[1], kXSlot);
+    // every incoming slot is armed for its first piece before the peer can send
+    for (int i = 0; i < kInSlots; ++i) mbar_arrive_expect_tx(&bars.x_full[i], kXSlot);
   }
   if (warp == 2) {
     tmem_alloc(&bars.tmem_base, kTmemCols);
@@ -334,6 +340,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort_flag;
+#ifdef MLA_TRACE
+  if (tid == 0 && blockIdx.x < 512) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_cta_time[blockIdx.x][0] = smid;
+    g_cta_time[blockIdx.x][1] = (long long)globaltimer_ns();
+  }
+#endif
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (cache tiles)
@@ -341,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     wk.init(p, unit, nunits);
     Seg sg;
     int gt = 0;
-    int issued[4] = {0, 0, 0, 0};
+    int issued[C::kStages] = {};
     bool ok = true;
     const int rows_box = min(p.page, kKeysT);
     const int subs = kKeysT / rows_box;
@@ -408,7 +422,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       volatile int dummy = 0;
       for (int s = 0; s < C::kStages; ++s)
-        if (issued[s] > 0) mbar_wait(&bars.kv_full[s], (issued[s] - 1) & 1, &dummy);
+        if (issued[s] > 0 && !mbar_wait(&bars.kv_full[s], (issued[s] - 1) & 1, &dummy))
+          atomicOr(&g_tc_err, kErrTimeout);   // a copy that never landed: report, never pass silently
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer. The whole
@@ -418,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Walker wk;
     wk.init(p, unit, nunits);
     Seg sg;
-    int gt = 0, seg_i = 0;
+    int gt = 0, seg_i = 0, full_i = 0;   // unit tile, segment, segment among those with tiles
     bool ok = true;
     constexpr uint32_t id_qk = idesc_bf16(kRows, kKeysT, false, false);
     constexpr uint32_t id_pv = idesc_bf16(kRows, 256, false, true);
@@ -427,7 +442,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t ones_base = smem_u32(smem + C::kOffOnes);
     while (ok && wk.next(p, sg)) {
       const int nt = ntiles(sg);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_ready, seg_i & 1, abort));
+      if (nt == 0) {
+        // an empty segment completes once the epilogue has read the previous segment's O: one
+        // completion per epilogue, so the softmax group's parity waits never fall two behind
+        ok = __all_sync(0xffffffffu, seg_i == 0 || mbar_wait(&bars.o_empty, (seg_i - 1) & 1, abort));
+        if (!ok) break;
+        umma_commit_elect(&bars.seg_done);
+        ++seg_i;
+        continue;
+      }
+      // its Q is in TMEM (q_ready completes one phase per segment with tiles; the exchange
+      // group loads the next Q only after consuming every S of this one, so no parity aliasing)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_ready, full_i & 1, abort));
       int qk = 0, pv = 0;
       uint64_t last = globaltimer_ns();
       uint32_t spins = 0;
@@ -490,20 +516,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (nt == 0) umma_commit_elect(&bars.seg_done);
       gt += nt;
       ++seg_i;
+      ++full_i;
     }
     if (!ok && lane == 0) set_abort(bars, peer);
     __syncwarp();
     // every MMA this warp issued is complete before the TMEM is released
     umma_commit_elect(&bars.mma_final);
     volatile int dummy = 0;
-    mbar_wait(&bars.mma_final, 0, &dummy);
+    if (!mbar_wait(&bars.mma_final, 0, &dummy) && lane == 0) atomicOr(&g_tc_err, kErrTimeout);
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ forwarder: releases the
-    // incoming buffers to the peer once the softmax group has read them
+    // incoming slots to the peer once the softmax group has read them (a relaxed arrive: the
+    // reads it answers for were completed by the softmax group's barrier before it was asked)
     if (lane == 0) {
       Walker wk;
       wk.init(p, unit, nunits);
@@ -512,12 +539,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && wk.next(p, sg)) {
         const int nt = ntiles(sg);
-        for (int j = 0; ok && j < nt; ++j) {
-          const int t = gt + j, b = t & 1;
-          ok = mbar_wait(&bars.xin_free[b], (t >> 1) & 1, abort);
-          if (ok) mbar_arrive_remote(&bars.x_empty[b], peer);
+        for (int q = 2 * gt; ok && q < 2 * (gt + nt); ++q) {
+          const int rs = q % kInSlots;
+          ok = mbar_wait(&bars.xin_free[rs], (q / kInSlots) & 1, abort);
+          if (ok) mbar_arrive_remote_relaxed(&bars.x_empty[rs], peer);
 #ifdef MLA_TRACE
-          if (unit == 0 && t < 512) g_trace2[rank][4][t] = clock64();
+          if (unit == 0 && q < 1024 && (q & 1)) g_trace2[rank][4][q >> 1] = clock64();
 #endif
         }
         gt += nt;
@@ -543,14 +570,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nt = ntiles(sg);
       const bool row_valid = row < p.H * p.tpt && t_in_tile < sg.ntok;
       const int limit = row_valid ? min(sg.k1, sg.pos0 + t_in_tile + 1) : 0;
-      // ---- this CTA's Q columns of the row tile into TMEM, once the previous
-      // segment's MMAs are done (two bf16 per column, the even one low)
-      if (seg_i > 0) {
-        ok = group_all(mbar_wait(&bars.seg_done, (seg_i - 1) & 1, abort));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      {
+      // ---- this CTA's Q columns of the row tile into TMEM (two bf16 per column, the even
+      // one low), for segments with tiles only (q_ready completes one phase per such segment).
+      // The group has consumed every S so far, so every QK MMA that read the old Q is
+      // complete: no wait for the old segment's PVs.
+      tc_fence_after();
+      if (nt > 0) {
         const __nv_bfloat16* qrow = p.q + (int64_t)(sg.tok0 + t_in_tile) * p.q_s0 + (int64_t)head * p.q_s1;
         for (int c = 0; c < 4 + (kRope ? 1 : 0); ++c) {
           // latent chunk c: 64 values; chunk 4: this CTA's 32 rope values (upper columns zero)
@@ -575,15 +600,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       bool sent = true;   // row 0: its last push went out
       for (int j = 0; ok && j < nt; ++j) {
-        const int t = gt + j, b = t & 1;
-        // ---- one group decision per tile: S(t) is in TMEM, outgoing slot b is free (the
-        // softmax group has read tile t-2 from it, and the push of tile t-2 has left it: all
-        // pushes but the latest, tile t-1's, have been read) and row 0's last push went out
-        bool mine = mbar_wait(&bars.s_full, t & 1, abort) &&
-                    mbar_wait(&bars.xloc_free[b], ((t >> 1) & 1) ^ 1, abort);
+        const int t = gt + j;
+        // ---- one group decision per tile: S(t) is in TMEM, the outgoing slot is free (the
+        // softmax group has read tile t-1 from it and both its pushes have left it) and row
+        // 0's last push went out
+        bool mine = mbar_wait(&bars.s_full, t & 1, abort) && mbar_wait(&bars.xloc_free, (t & 1) ^ 1, abort);
         if (row == 0) {
           mine = mine && sent;
-          bulk_wait_read_but_last();
+          bulk_wait_read_all();
         }
         ok = group_all(mine);
         if (!ok) break;
@@ -620,25 +644,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                          ex2_approx(fmaf(sv[k + 1], p.scale_log2, neg_c)));
           ek[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        // ---- into outgoing slot b, then to the peer once its incoming slot b is free
-        unsigned char* slot = sXloc + b * kXSlot;
+        // ---- both pieces into the outgoing slot (row r's 64 bytes of a piece as four 16-byte
+        // chunks, rotated by (r / 2) % 4 against bank conflicts), then each piece to the peer
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(slot + row * 128 + ((ch ^ (row & 7)) << 4)) =
-              make_uint4(ek[4 * ch], ek[4 * ch + 1], ek[4 * ch + 2], ek[4 * ch + 3]);
-        reinterpret_cast<float*>(slot + kESlotBytes)[row] = c;
+        for (int h = 0; h < 2; ++h) {
+          unsigned char* piece = sXloc + h * kXSlot;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            *reinterpret_cast<uint4*>(piece + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4)) =
+                make_uint4(ek[16 * h + 4 * ch], ek[16 * h + 4 * ch + 1], ek[16 * h + 4 * ch + 2],
+                           ek[16 * h + 4 * ch + 3]);
+          reinterpret_cast<float*>(piece + kESlotBytes)[row] = c;
+        }
         fence_proxy_async_smem();
         named_bar(kXchgBar, 128);
         MLA_TRACE_AT(4, t);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.own_ready[b]);
+        if (lane == 0) mbar_arrive(&bars.own_ready);
         if (row == 0) {
-          // the peer's incoming slot b is free once it has consumed tile t - 2
-          sent = mbar_wait<true>(&bars.x_empty[b], ((t >> 1) & 1) ^ 1, abort);
-          MLA_TRACE2_AT(0, t);
-          if (sent) {
-            bulk_copy_to_peer(peer_rem0 + b * kXSlot, slot, kXSlot, peer_xfull0 + b * 8);
-            bulk_commit_group();
+          for (int h = 0; sent && h < 2; ++h) {
+            // piece q goes to the peer's incoming slot q % 3, free once it has read piece q - 3
+            const int q = 2 * t + h, rs = q % kInSlots;
+            sent = mbar_wait<true>(&bars.x_empty[rs], ((q / kInSlots) & 1) ^ 1, abort);
+            if (h == 0) MLA_TRACE2_AT(0, t);
+            if (sent) {
+              bulk_copy_to_peer(peer_rem0 + rs * kXSlot, sXloc + h * kXSlot, kXSlot, peer_xfull0 + rs * 8);
+              bulk_commit_group();
+            }
           }
         }
       }
@@ -666,57 +698,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool row_valid = row < p.H * p.tpt && t_in_tile < sg.ntok;
       float m = -CUDART_INF_F;             // running reference max (base 2); the denominator is in TMEM
       for (int j = 0; ok && j < nt; ++j) {
-        const int g = gt + j, b = g & 1;
+        const int g = gt + j;
+        // ---- the own tile: both pieces and c at once, which frees the outgoing slot early
         MLA_TRACE2_AT(1, g);
-        const bool own_ok = mbar_wait(&bars.own_ready[b], (g >> 1) & 1, abort);
+        ok = group_all(mbar_wait(&bars.own_ready, g & 1, abort));
         MLA_TRACE2_AT(2, g);
-        ok = group_all(own_ok && mbar_wait<true>(&bars.x_full[b], (g >> 1) & 1, abort));
-        MLA_TRACE2_AT(3, g);
         if (!ok) break;
-        const unsigned char* own = sXloc + b * kXSlot;
-        const unsigned char* rem = sXrem + b * kXSlot;
-        uint4 eo[8], er[8];
+        uint4 eo[8];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          eo[ch] = *reinterpret_cast<const uint4*>(own + row * 128 + ((ch ^ (row & 7)) << 4));
-          er[ch] = *reinterpret_cast<const uint4*>(rem + row * 128 + ((ch ^ (row & 7)) << 4));
-        }
-        const float c_own = reinterpret_cast<const float*>(own + kESlotBytes)[row];
-        const float c_rem = reinterpret_cast<const float*>(rem + kESlotBytes)[row];
-        // both slots are read: re-arm the incoming one, release it to the peer (through
-        // warp 3) and hand the outgoing one back to the exchange group
-        named_bar(kSoftmaxBar, 128);
-        if (row == 0) {
-          mbar_arrive_expect_tx(&bars.x_full[b], kXSlot);
-          mbar_arrive(&bars.xin_free[b]);
-          mbar_arrive(&bars.xloc_free[b]);
-        }
-        MLA_TRACE2_AT(5, g);
-        // ---- tile upper bound M = c_0 + c_1; IEEE addition and multiplication commute, so
-        // own-then-peer operands give both CTAs bit-identical M and P without knowing rank
-        const float M = (c_own == -CUDART_INF_F || c_rem == -CUDART_INF_F) ? -CUDART_INF_F : c_own + c_rem;
-        float alpha = 1.f;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            eo[4 * h + ch] = *reinterpret_cast<const uint4*>(sXloc + h * kXSlot + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+        const float c_own = reinterpret_cast<const float*>(sXloc + kESlotBytes)[row];
+        float alpha = 1.f, factor = 0.f;
         bool rescale_o = false;
-        if (M > m + kLazyRescale || (m == -CUDART_INF_F && M > -CUDART_INF_F)) {
-          alpha = m == -CUDART_INF_F ? 0.f : exp2_int(m - M);
-          rescale_o = (m != -CUDART_INF_F) && j > 0;
-          m = M;
-        }
-        const float factor = M == -CUDART_INF_F ? 0.f : exp2_int(M - m);
-        MLA_TRACE2_AT(6, g);
-        // ---- P = (E_own * E_peer) * 2^(M - m): the same value in both CTAs
-        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(eo);
-        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(er);
-        // packed bf16 products: E_own * E_peer rounded once; the factor is an exact power of two
-        const __nv_bfloat162 f2 = __float2bfloat162_rn(factor);
         uint32_t pk[32];
+        // ---- the peer's pieces, each as soon as it lands
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const __nv_bfloat162 e = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&w0[k]),
-                                           *reinterpret_cast<const __nv_bfloat162*>(&w1[k]));
-          const __nv_bfloat162 q = __hmul2(e, f2);
-          pk[k] = *reinterpret_cast<const uint32_t*>(&q);
+        for (int h = 0; h < 2; ++h) {
+          const int q = 2 * g + h, rs = q % kInSlots;
+          ok = group_all(mbar_wait<true>(&bars.x_full[rs], (q / kInSlots) & 1, abort));
+          if (h == 0) MLA_TRACE2_AT(3, g);
+          if (!ok) break;
+          const unsigned char* rem = sXrem + rs * kXSlot;
+          uint4 er[4];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            er[ch] = *reinterpret_cast<const uint4*>(rem + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+          const float c_rem = reinterpret_cast<const float*>(rem + kESlotBytes)[row];
+          // read: re-arm the incoming slot and release it to the peer (through warp 3); after
+          // the first piece the outgoing slot goes back to the exchange group
+          named_bar(kSoftmaxBar, 128);
+          if (row == 0) {
+            mbar_arrive_expect_tx(&bars.x_full[rs], kXSlot);
+            mbar_arrive(&bars.xin_free[rs]);
+            if (h == 0) mbar_arrive(&bars.xloc_free);
+          }
+          if (h == 0) {
+            MLA_TRACE2_AT(5, g);
+            // ---- tile upper bound M = c_0 + c_1; IEEE addition and multiplication commute, so
+            // own-then-peer operands give both CTAs bit-identical M and P without knowing rank
+            const float M = (c_own == -CUDART_INF_F || c_rem == -CUDART_INF_F) ? -CUDART_INF_F : c_own + c_rem;
+            if (M > m + kLazyRescale || (m == -CUDART_INF_F && M > -CUDART_INF_F)) {
+              alpha = m == -CUDART_INF_F ? 0.f : exp2_int(m - M);
+              rescale_o = (m != -CUDART_INF_F) && j > 0;
+              m = M;
+            }
+            factor = M == -CUDART_INF_F ? 0.f : exp2_int(M - m);
+            MLA_TRACE2_AT(6, g);
+          }
+          // ---- P = (E_own * E_peer) * 2^(M - m): packed bf16 products rounded once (the
+          // factor is an exact power of two), the same value in both CTAs
+          const __nv_bfloat162 f2 = __float2bfloat162_rn(factor);
+          const uint32_t* w0 = reinterpret_cast<const uint32_t*>(eo + 4 * h);
+          const uint32_t* w1 = reinterpret_cast<const uint32_t*>(er);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const __nv_bfloat162 e = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&w0[k]),
+                                             *reinterpret_cast<const __nv_bfloat162*>(&w1[k]));
+            const __nv_bfloat162 pq = __hmul2(e, f2);
+            pk[16 * h + k] = *reinterpret_cast<const uint32_t*>(&pq);
+          }
         }
+        if (!ok) break;
         MLA_TRACE_AT(7, g);
         // ---- P(g) replaces P(g-1) in TMEM once PV(g-1) is done; O is rescaled then too
         if (g > 0) {
@@ -830,6 +875,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && bars.abort_flag) atomicOr(&g_tc_err, kErrTimeout);
+#ifdef MLA_TRACE
+  if (tid == 0 && blockIdx.x < 512) g_cta_time[blockIdx.x][2] = (long long)globaltimer_ns();
+#endif
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -1021,8 +1069,10 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
 
 #ifdef MLA_TRACE
 extern "C" int mla_debug_trace(long long* host) {
-  const int e = (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
-  return e ? e : (int)cudaMemcpyFromSymbol(host + 2 * 8 * 512, g_trace2, sizeof(g_trace2));
+  int e = (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
+  if (!e) e = (int)cudaMemcpyFromSymbol(host + 2 * 8 * 512, g_trace2, sizeof(g_trace2));
+  if (!e) e = (int)cudaMemcpyFromSymbol(host + 4 * 8 * 512, g_cta_time, sizeof(g_cta_time));
+  return e;
 }
 #endif
 

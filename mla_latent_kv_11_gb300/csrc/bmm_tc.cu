@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     volatile int dummy = 0;
     for (int s = 0; s < kStages; ++s)
-      if (issued[s] > 0) mbar_wait(&full[s], (issued[s] - 1) & 1, &dummy);
+      if (issued[s] > 0 && !mbar_wait(&full[s], (issued[s] - 1) & 1, &dummy)) atomicOr(&g_bmm_err, kErrTimeout);
   } else if (warp == 1) {
     // MMA issuer: the converged warp walks the k-steps, one elected lane issues
     constexpr uint32_t idesc = idesc_bf16(kBM, kBN, false, true);
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     umma_commit_elect(done);
     volatile int dummy = 0;
-    mbar_wait(done, 0, &dummy);
+    if (!mbar_wait(done, 0, &dummy) && lane == 0) atomicOr(&g_bmm_err, kErrTimeout);
   }
   __syncwarp();
   // epilogue: every thread owns one row (TMEM lane) of the tile

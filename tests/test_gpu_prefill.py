@@ -77,3 +77,29 @@ def test_prefill_nope_full_size_sampled(mla):
                                  (page * L, L, 1), L, R, table, scale, rows_wanted=rows)
     check_close(got[rows], want, "bf16", "nope prefill (sampled rows)")
     assert np.max(np.abs(lse[rows] - want_lse)) < 1e-2
+
+
+@pytest.mark.parametrize("H,R", [(128, 64), (64, 0)])
+def test_prefill_tensor_core_rows_without_keys(mla, H, R):
+    # The tensor-core shapes with sequences whose query rows see no cache row at all (kv_len 0,
+    # or more queries than cached rows), back to back, next to ordinary ones and an empty query
+    # range: such rows give o = 0 and lse = -inf, and the rows after them must be right.
+    L, page = 512, 64
+    E = L + R
+    q_lens = [5, 3, 70, 1, 10, 0, 130]
+    kv_lens = [0, 0, 70, 1, 4, 10, 300]
+    table, nb = _tables(kv_lens, page, 91)
+    cache = mi.encode(mi.draw("normal", 92, nb * page * E, 0.5), "bf16").reshape(nb, page, E)
+    T = sum(q_lens)
+    q = mi.encode(mi.draw("normal", 93, T * H * E, 0.5), "bf16").reshape(T, H, E)
+    scale = 1.0 / math.sqrt(192)
+    o, lse, cu = run_prefill(mla, q, cache, table, q_lens, kv_lens, "bf16", L, R, scale)
+    storage = mi.decode_f64(cache.reshape(-1), "bf16")
+    want, want_lse = orc.prefill(mi.decode_f64(q, "bf16"), cu, np.array(kv_lens), storage, 0, page,
+                                 (page * E, E, 1), L, R, table, scale)
+    got = to_f64(o)
+    check_close(got, want, "bf16", f"prefill rows without keys H={H} R={R}")
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.max(np.abs(lse[fin] - want_lse[fin])) < 1.2e-2   # ln(1 + 3 * 2^-8): see the decode tests
+    assert np.all(got[~fin.all(axis=1)] == 0)
