@@ -2,15 +2,16 @@
 // (any head count, any dtype) decode and prefill kernels.
 //
 // Schedule. The batch's context is cut into tiles of kTile rows; sequence b
-// owns ceil(len_b / kTile) tiles and tile_prefix is their prefix sum. With
-// W = min(units, total) work units, unit w takes the contiguous global range
-//   [floor(w*total/W), floor((w+1)*total/W)),
-// so every unit gets the same number of tiles (at least one) whatever the
-// length mix; units past W have nothing to do. A unit
-// that covers a whole sequence writes the final output; a sequence cut across
-// n > 1 units gets n partial slots (normalised o and LSE), merged afterwards by
-// the combine kernel. The schedule depends only on the lengths and W: results
-// are run-to-run bit-identical and do not depend on the cache strides.
+// owns ceil(len_b / kTile) tiles and tile_prefix is their prefix sum. The W
+// work units take contiguous global tile ranges [unit_tile[w], unit_tile[w+1])
+// of equal cost, where a sequence costs its tiles plus kSeqCost for its start
+// (starting a sequence drains and refills the attention pipeline: about as
+// long as kSeqCost tiles), so units that hold many short sequences get fewer
+// tiles; a unit may get none. A unit that covers a whole sequence writes the
+// final output; a sequence cut across n > 1 units gets n partial slots
+// (normalised o and LSE), merged afterwards by the combine kernel. The
+// schedule depends only on the lengths and W: results are run-to-run
+// bit-identical and do not depend on the cache strides.
 //
 // SIMT attention. One CTA holds the queries of a group of up to 16 heads of one
 // token in shared memory (fp32), streams the key rows of its range in tiles of
@@ -73,12 +74,17 @@ __device__ __forceinline__ int clamp_len(const int32_t* seq_lens, int b, int cap
   return n;
 }
 
-__device__ __forceinline__ int unit_begin(int w, int total, int W) {
-  return (int)(((long long)w * total) / W);
-}
-// The unit whose range holds global tile t (the last unit with begin <= t).
-__device__ __forceinline__ int unit_of(int t, int total, int W) {
-  return (int)((((long long)t + 1) * W - 1) / total);
+constexpr int kSeqCost = 6;   // cost of starting a sequence, in tiles (measured)
+
+// The unit whose range holds global tile t: the last w with unit_tile[w] <= t (units with
+// empty ranges sit only at sequence starts, so this is never an empty unit).
+__device__ __forceinline__ int unit_of(const int32_t* unit_tile, int W, int t) {
+  int lo = 0, hi = W - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (unit_tile[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __restrict__ seq_lens,
@@ -87,7 +93,9 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   __shared__ int carry_sh;
   if (threadIdx.x == 0) carry_sh = 0;
   __syncthreads();
-  // pass 1: tile prefix
+  __shared__ int starts_sh;
+  // pass 1: tile prefix, and (in first_unit, until pass 2) the number of sequences with
+  // tiles before b
   for (int base = 0; base < B; base += 1024) {
     const int b = base + threadIdx.x;
     const int n = b < B ? (clamp_len(seq_lens, b, cap) + kTile - 1) / kTile : 0;
@@ -99,10 +107,52 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     if (threadIdx.x == 0) carry_sh = carry + tot;
     __syncthreads();
   }
-  if (threadIdx.x == 0) s.tile_prefix[B] = carry_sh;
+  if (threadIdx.x == 0) {
+    s.tile_prefix[B] = carry_sh;
+    starts_sh = 0;
+  }
   __syncthreads();
   const int total = carry_sh;
-  const int W = min(s.units, total);  // every unit in use gets at least one tile
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + threadIdx.x;
+    const int nz = b < B && s.tile_prefix[b + 1] > s.tile_prefix[b] ? 1 : 0;
+    int tot;
+    const int ex = block_exclusive_scan(nz, warp_tot, &tot);
+    const int carry = starts_sh;
+    if (b < B) s.first_unit[b] = carry + ex;
+    __syncthreads();
+    if (threadIdx.x == 0) starts_sh = carry + tot;
+    __syncthreads();
+  }
+  const int starts = starts_sh;
+  const int W = s.units;
+  // unit boundaries: unit w < We = min(W, total) starts at cost floor(w * C / We),
+  // C = total + kSeqCost * starts; sequence b spans costs [cost_b, cost_b + (kSeqCost if it
+  // has tiles) + tiles_b) with cost_b = tile_prefix[b] + kSeqCost * (sequences with tiles
+  // before b). C >= We, so boundaries inside a sequence's tiles are distinct; units from We
+  // on get empty ranges at the end
+  const long long C = (long long)total + (long long)kSeqCost * starts;
+  const int We = min(W, total);
+  for (int w = threadIdx.x; w <= W; w += blockDim.x) {
+    if (w >= We) {
+      s.unit_tile[w] = total;
+      continue;
+    }
+    const long long x = ((long long)w * C) / We;
+    int lo = 0, hi = B;   // the last b with cost_b <= x (cost_B = C)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      const long long cm = s.tile_prefix[mid] + (long long)kSeqCost * (mid < B ? s.first_unit[mid] : starts);
+      if (cm <= x) lo = mid; else hi = mid - 1;
+    }
+    int t = total;
+    if (lo < B) {
+      const int tiles = s.tile_prefix[lo + 1] - s.tile_prefix[lo];
+      const long long into = x - (s.tile_prefix[lo] + (long long)kSeqCost * s.first_unit[lo]) - (tiles > 0 ? kSeqCost : 0);
+      t = s.tile_prefix[lo] + (int)(into < 0 ? 0 : (into > tiles ? tiles : into));
+    }
+    s.unit_tile[w] = t;
+  }
   __syncthreads();
   if (threadIdx.x == 0) carry_sh = 0;
   __syncthreads();
@@ -113,8 +163,8 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     if (b < B) {
       const int t0 = s.tile_prefix[b], t1 = s.tile_prefix[b + 1];
       if (t1 > t0) {
-        fu = unit_of(t0, total, W);
-        np = unit_of(t1 - 1, total, W) - fu + 1;
+        fu = unit_of(s.unit_tile, W, t0);
+        np = unit_of(s.unit_tile, W, t1 - 1) - fu + 1;
       }
       s.first_unit[b] = fu;
       s.npieces[b] = np;
@@ -255,11 +305,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
     DecodeSched s) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const SimtSmem sm = simt_smem(smem_raw, L + R);
-  const int total = s.tile_prefix[B];
-  const int W = min(s.units, total), w = blockIdx.x;
-  if (w >= W) return;
+  const int w = blockIdx.x;
+  const int t0 = s.unit_tile[w], t1 = s.unit_tile[w + 1];
+  if (t0 >= t1) return;
   const int h0 = blockIdx.y * kHeads, hn = min(kHeads, H - h0);
-  const int t0 = unit_begin(w, total, W), t1 = unit_begin(w + 1, total, W);
   const int E = L + R;
   // first sequence: the last b with tile_prefix[b] <= t0
   int lo = 0, hi = B;

@@ -200,14 +200,12 @@ struct Walker {
     nunits = nunits_;
     active = true;
     if (p.mode == 0) {
-      const int total = p.sched.tile_prefix[p.B];
-      const int W = min(p.sched.units, total);
-      if (unit >= W) {
+      t = p.sched.unit_tile[unit];
+      t1 = p.sched.unit_tile[unit + 1];
+      if (t >= t1) {
         active = false;
         return;
       }
-      t = (int)(((long long)unit * total) / W);
-      t1 = (int)(((long long)(unit + 1) * total) / W);
       int lo = 0, hi = p.B;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;

@@ -41,6 +41,7 @@ struct DecodeSched {
   int32_t* first_unit;   // [B]   work unit holding the first tile of b
   int32_t* npieces;      // [B]   work units touching b (0 for an empty sequence)
   int32_t* piece_base;   // [B]   first partial slot of b (if npieces[b] > 1)
+  int32_t* unit_tile;    // [units+1] first global tile of each work unit (the last entry: total)
   float* part_o;         // [max_pieces, H, L] normalised partial outputs
   float* part_lse;       // [max_pieces, H]    their natural-log LSE
   int32_t units;         // number of work units W
@@ -49,7 +50,7 @@ struct DecodeSched {
 
 // Workspace layout of mla_decode for (B, H, L, units).
 struct DecodeWsLayout {
-  size_t off_prefix, off_first, off_np, off_base, off_part_o, off_part_lse, total;
+  size_t off_prefix, off_first, off_np, off_base, off_unit, off_part_o, off_part_lse, total;
 };
 DecodeWsLayout decode_ws_layout(int64_t B, int64_t H, int64_t L, int64_t units);
 DecodeSched decode_sched_from_ws(void* ws, const DecodeWsLayout& lay, int32_t B, int32_t units);
