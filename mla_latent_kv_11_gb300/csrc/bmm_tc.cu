@@ -2,8 +2,10 @@
 // bf16 with fp32 accumulation (tcgen05 + TMEM + TMA), for K a multiple of 64
 // and N a multiple of 128.
 //
-// One CTA computes a 128 x BN tile (BN = 256, or 128 when N is not a multiple
-// of 256) of one head g. TMA 3-D tensor maps read the operands straight from
+// One CTA computes a 128 x BN tile of one head g: BN = 512 when N is a
+// multiple of 512 and one tile per head fits in a single wave of CTAs (the
+// decode absorb: 128 heads x 64 tokens x 512), else 256, else 128. A 512-wide
+// tile accumulates in all 512 TMEM columns through two N=256 MMAs per k-step. TMA 3-D tensor maps read the operands straight from
 // their strided views (the usual transposed [H,B,P] operand and [H,B,L]
 // output cost nothing extra): A tiles are K-major [128 rows x 64 k] boxes,
 // B tiles are [64 k x 64 n] boxes used as an MN-major operand. A 4-stage ring
@@ -30,12 +32,14 @@ __device__ unsigned g_bmm_err = 0;
 
 constexpr int kThreads = 128;
 constexpr int kBM = 128, kBK = 64;
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBBox = kBK * 64 * 2;      // 8 KB: 64 k-rows x 64 n
 
 template <int kBN>
 struct BmmCfg {
+  static constexpr int kStages = kBN > 256 ? 2 : 4;
+  static constexpr int kNHalf = kBN > 256 ? 256 : kBN;      // N of one MMA
+  static constexpr uint32_t kTmemCols = kBN > 256 ? 512 : 256;
   static constexpr int kBBytes = (kBN / 64) * kBBox;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOff = kStages * kStageBytes;
@@ -57,8 +61,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* empty = full + kStages;
-  uint64_t* done = empty + kStages;
+  uint64_t* empty = full + C::kStages;
+  uint64_t* done = empty + C::kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -67,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ksteps = K / kBK;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -76,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -89,10 +93,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // producer
     tma_prefetch_desc(&amap);
     tma_prefetch_desc(&bmap);
-    int issued[kStages] = {0, 0, 0, 0};
+    int issued[C::kStages] = {};
     for (int ks = 0; ks < ksteps; ++ks) {
-      const int s = ks % kStages;
-      if (!mbar_wait(&empty[s], ((ks / kStages) & 1) ^ 1, abort)) break;
+      const int s = ks % C::kStages;
+      if (!mbar_wait(&empty[s], ((ks / C::kStages) & 1) ^ 1, abort)) break;
       unsigned char* st = smem + s * C::kStageBytes;
       mbar_arrive_expect_tx(&full[s], C::kStageBytes);
       tma_load_3d(st, &amap, &full[s], ks * kBK, m0, g);
@@ -100,22 +104,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++issued[s];
     }
     volatile int dummy = 0;
-    for (int s = 0; s < kStages; ++s)
+    for (int s = 0; s < C::kStages; ++s)
       if (issued[s] > 0 && !mbar_wait(&full[s], (issued[s] - 1) & 1, &dummy)) atomicOr(&g_bmm_err, kErrTimeout);
   } else if (warp == 1) {
     // MMA issuer: the converged warp walks the k-steps, one elected lane issues
-    constexpr uint32_t idesc = idesc_bf16(kBM, kBN, false, true);
+    constexpr uint32_t idesc = idesc_bf16(kBM, C::kNHalf, false, true);
     bool ok = true;
     for (int ks = 0; ks < ksteps && ok; ++ks) {
-      const int s = ks % kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (ks / kStages) & 1, abort));
+      const int s = ks % C::kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (ks / C::kStages) & 1, abort));
       if (!ok) break;
       tc_fence_after();
       const uint32_t a = smem_u32(smem + s * C::kStageBytes), b = a + kABytes;
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk)
-        umma_bf16_elect(tmem, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(b + kk * 16 * 128, kBBox, 1024), idesc,
-                        (ks | kk) ? 1u : 0u);
+#pragma unroll
+        for (int h = 0; h < kBN / C::kNHalf; ++h)   // N halves: accumulators at columns 0 and 256
+          umma_bf16_elect(tmem + h * C::kNHalf, sdesc_sw128(a + kk * 32, 16, 1024),
+                          sdesc_sw128(b + h * (C::kNHalf / 64) * kBBox + kk * 16 * 128, kBBox, 1024), idesc,
+                          (ks | kk) ? 1u : 0u);
       umma_commit_elect(&empty[s]);
     }
     umma_commit_elect(done);
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -221,11 +228,15 @@ bool bmm_tc_supported(mla_dtype dt, const View3& out, const View3& a, const View
 
 cudaError_t launch_bmm_tc(const View3& out, const View3& a, const View3& b, cudaStream_t st) {
   const int G = (int)a.n0, M = (int)a.n1, K = (int)a.n2, N = (int)b.n2;
-  const int bn = N % 256 == 0 ? 256 : 128;
+  const int tiles_per_head_m = (M + kBM - 1) / kBM;
+  const int bn = (N % 512 == 0 && (long long)G * tiles_per_head_m <= device_sm_count()) ? 512
+                 : N % 256 == 0                                                  ? 256
+                                                                                 : 128;
   CUtensorMap am, bm, cm;
   if (!map3(&am, a.data, K, M, G, a.s1, a.s0, 64, kBM) || !map3(&bm, b.data, N, K, G, b.s1, b.s0, 64, kBK) ||
       !map3(&cm, out.data, N, M, G, out.s1, out.s0, 64, kBM))
     return cudaErrorInvalidValue;
+  if (bn == 512) return launch<512>(am, bm, cm, G, M, N, K, st);
   return bn == 256 ? launch<256>(am, bm, cm, G, M, N, K, st) : launch<128>(am, bm, cm, G, M, N, K, st);
 }
 
