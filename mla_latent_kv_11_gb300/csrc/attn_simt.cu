@@ -87,45 +87,54 @@ __device__ __forceinline__ int unit_of(const int32_t* unit_tile, int W, int t) {
   return lo;
 }
 
+// The prefix arrays live in shared memory while the batch fits (the binary searches then cost
+// no global round trips); larger batches work on the workspace arrays directly.
+constexpr int kSchedSmemSeqs = 2048;
+constexpr int kSchedSmemUnits = 1024;
+
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __restrict__ seq_lens,
                                                                int B, int cap, DecodeSched s) {
   __shared__ int warp_tot[32];
-  __shared__ int carry_sh;
-  if (threadIdx.x == 0) carry_sh = 0;
+  __shared__ int carry_sh, starts_sh;
+  __shared__ int pre_sh[kSchedSmemSeqs + 1], nz_sh[kSchedSmemSeqs + 1], ut_sh[kSchedSmemUnits + 1];
+  const int W = s.units;
+  const bool seqs_in_smem = B <= kSchedSmemSeqs, units_in_smem = W <= kSchedSmemUnits;
+  int* pre = seqs_in_smem ? pre_sh : s.tile_prefix;   // tile prefix
+  int* nzb = seqs_in_smem ? nz_sh : s.first_unit;     // sequences with tiles before b
+  int* ut = units_in_smem ? ut_sh : s.unit_tile;      // unit boundaries
+  if (threadIdx.x == 0) {
+    carry_sh = 0;
+    starts_sh = 0;
+  }
   __syncthreads();
-  __shared__ int starts_sh;
-  // pass 1: tile prefix, and (in first_unit, until pass 2) the number of sequences with
-  // tiles before b
+  // pass 1: tile prefix
   for (int base = 0; base < B; base += 1024) {
     const int b = base + threadIdx.x;
     const int n = b < B ? (clamp_len(seq_lens, b, cap) + kTile - 1) / kTile : 0;
     int tot;
     const int ex = block_exclusive_scan(n, warp_tot, &tot);
     const int carry = carry_sh;
-    if (b < B) s.tile_prefix[b] = carry + ex;
+    if (b < B) pre[b] = carry + ex;
     __syncthreads();
     if (threadIdx.x == 0) carry_sh = carry + tot;
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    s.tile_prefix[B] = carry_sh;
-    starts_sh = 0;
-  }
+  if (threadIdx.x == 0) pre[B] = carry_sh;
   __syncthreads();
   const int total = carry_sh;
+  // the number of sequences with tiles before each b
   for (int base = 0; base < B; base += 1024) {
     const int b = base + threadIdx.x;
-    const int nz = b < B && s.tile_prefix[b + 1] > s.tile_prefix[b] ? 1 : 0;
+    const int nz = b < B && pre[b + 1] > pre[b] ? 1 : 0;
     int tot;
     const int ex = block_exclusive_scan(nz, warp_tot, &tot);
     const int carry = starts_sh;
-    if (b < B) s.first_unit[b] = carry + ex;
+    if (b < B) nzb[b] = carry + ex;
     __syncthreads();
     if (threadIdx.x == 0) starts_sh = carry + tot;
     __syncthreads();
   }
   const int starts = starts_sh;
-  const int W = s.units;
   // unit boundaries: unit w < We = min(W, total) starts at cost floor(w * C / We),
   // C = total + kSeqCost * starts; sequence b spans costs [cost_b, cost_b + (kSeqCost if it
   // has tiles) + tiles_b) with cost_b = tile_prefix[b] + kSeqCost * (sequences with tiles
@@ -135,23 +144,23 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   const int We = min(W, total);
   for (int w = threadIdx.x; w <= W; w += blockDim.x) {
     if (w >= We) {
-      s.unit_tile[w] = total;
+      ut[w] = total;
       continue;
     }
     const long long x = ((long long)w * C) / We;
     int lo = 0, hi = B;   // the last b with cost_b <= x (cost_B = C)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      const long long cm = s.tile_prefix[mid] + (long long)kSeqCost * (mid < B ? s.first_unit[mid] : starts);
+      const long long cm = pre[mid] + (long long)kSeqCost * (mid < B ? nzb[mid] : starts);
       if (cm <= x) lo = mid; else hi = mid - 1;
     }
     int t = total;
     if (lo < B) {
-      const int tiles = s.tile_prefix[lo + 1] - s.tile_prefix[lo];
-      const long long into = x - (s.tile_prefix[lo] + (long long)kSeqCost * s.first_unit[lo]) - (tiles > 0 ? kSeqCost : 0);
-      t = s.tile_prefix[lo] + (int)(into < 0 ? 0 : (into > tiles ? tiles : into));
+      const int tiles = pre[lo + 1] - pre[lo];
+      const long long into = x - (pre[lo] + (long long)kSeqCost * nzb[lo]) - (tiles > 0 ? kSeqCost : 0);
+      t = pre[lo] + (int)(into < 0 ? 0 : (into > tiles ? tiles : into));
     }
-    s.unit_tile[w] = t;
+    ut[w] = t;
   }
   __syncthreads();
   if (threadIdx.x == 0) carry_sh = 0;
@@ -161,11 +170,15 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     const int b = base + threadIdx.x;
     int np = 0, fu = 0;
     if (b < B) {
-      const int t0 = s.tile_prefix[b], t1 = s.tile_prefix[b + 1];
+      const int t0 = pre[b], t1 = pre[b + 1];
       if (t1 > t0) {
-        fu = unit_of(s.unit_tile, W, t0);
-        np = unit_of(s.unit_tile, W, t1 - 1) - fu + 1;
+        fu = unit_of(ut, W, t0);
+        np = unit_of(ut, W, t1 - 1) - fu + 1;
       }
+    }
+    // every thread has read nzb (which may alias first_unit) before any first_unit is written
+    __syncthreads();
+    if (b < B) {
       s.first_unit[b] = fu;
       s.npieces[b] = np;
     }
@@ -177,6 +190,11 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     if (threadIdx.x == 0) carry_sh = carry + tot;
     __syncthreads();
   }
+  // the staged arrays out to the workspace
+  if (seqs_in_smem)
+    for (int b = threadIdx.x; b <= B; b += blockDim.x) s.tile_prefix[b] = pre_sh[b];
+  if (units_in_smem)
+    for (int w = threadIdx.x; w <= W; w += blockDim.x) s.unit_tile[w] = ut_sh[w];
 }
 
 // ---------------------------------------------------------------------------
@@ -402,7 +420,40 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
   const float* part = s.part_o + ((int64_t)base * H + h) * L;
   const bool vec = (L % 4 == 0) && ((o_s0 | o_s1) % 4 == 0) &&
                    (reinterpret_cast<uintptr_t>(o_lat) % (4 * sizeof(T)) == 0);
-  if (vec) {
+  if (vec && L == 512) {
+    // each lane owns four 16-byte chunks of the row; every load of a group of up to four
+    // pieces is issued before any of them is used, so the warp waits one memory latency
+    // per group instead of one per piece and chunk
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < np; i0 += 4) {
+      float4 v[4][4];
+      float wi[4];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const int i = i0 + ii;
+        const float li = i < np ? lse_p[(int64_t)i * H] : -CUDART_INF_F;
+        wi[ii] = li == -CUDART_INF_F ? 0.f : __expf(li - m);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          v[ii][k] = i < np ? *reinterpret_cast<const float4*>(part + i * pstride + lane * 4 + k * 128)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[k].x = fmaf(wi[ii], v[ii][k].x, acc[k].x);
+          acc[k].y = fmaf(wi[ii], v[ii][k].y, acc[k].y);
+          acc[k].z = fmaf(wi[ii], v[ii][k].z, acc[k].z);
+          acc[k].w = fmaf(wi[ii], v[ii][k].w, acc[k].w);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      store4<T>(o + lane * 4 + k * 128, make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv));
+  } else if (vec) {
     for (int c = lane * 4; c < L; c += 128) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int i = 0; i < np; ++i) {
