@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   __shared__ int warp_tot[32];
   __shared__ int carry_sh, starts_sh;
   __shared__ int pre_sh[kSchedSmemSeqs + 1], nz_sh[kSchedSmemSeqs + 1], ut_sh[kSchedSmemUnits + 1];
+  pdl_enter();
   const int W = s.units;
   const bool seqs_in_smem = B <= kSchedSmemSeqs, units_in_smem = W <= kSchedSmemUnits;
   int* pre = seqs_in_smem ? pre_sh : s.tile_prefix;   // tile prefix
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
     const int32_t* __restrict__ seq_lens, int cap, int B, int H, int L, int R, float scale,
     DecodeSched s) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  pdl_enter();
   const SimtSmem sm = simt_smem(smem_raw, L + R);
   const int w = blockIdx.x;
   const int t0 = s.unit_tile[w], t1 = s.unit_tile[w + 1];
@@ -395,6 +397,7 @@ template <typename T>
 __global__ void __launch_bounds__(128) decode_combine_kernel(
     T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
     int B, int H, int L, DecodeSched s) {
+  pdl_enter();
   const int b = blockIdx.x;
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (h >= H) return;
@@ -490,6 +493,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ kv_lens, int B, int H, int L,
     int R, float scale) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  pdl_enter();
   const SimtSmem sm = simt_smem(smem_raw, L + R);
   const int r = blockIdx.x;
   const int h0 = blockIdx.y * kHeads, hn = min(kHeads, H - h0);
@@ -531,8 +535,7 @@ void allow_smem(K k, size_t bytes) {
 cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
                                    int32_t page, const DecodeSched& s, cudaStream_t st) {
   const long long cap = (long long)max_blocks * page;
-  decode_schedule_kernel<<<1, 1024, 0, st>>>(seq_lens, B, (int)(cap > INT32_MAX ? INT32_MAX : cap), s);
-  return cudaGetLastError();
+  return launch_k(decode_schedule_kernel, 1, 1024, 0, st, seq_lens, B, (int)(cap > INT32_MAX ? INT32_MAX : cap), s);
 }
 
 cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
@@ -546,12 +549,12 @@ cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, con
   const size_t sm = simt_smem_bytes(L + R);
   if (dt == MLA_F32) {
     allow_smem(decode_split_simt_kernel<float>, sm);
-    decode_split_simt_kernel<float><<<grid, kThreads, sm, st>>>(
+    return launch_k(decode_split_simt_kernel<float>, grid, kThreads, sm, st,
         (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
         block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s);
   } else {
     allow_smem(decode_split_simt_kernel<__nv_bfloat16>, sm);
-    decode_split_simt_kernel<__nv_bfloat16><<<grid, kThreads, sm, st>>>(
+    return launch_k(decode_split_simt_kernel<__nv_bfloat16>, grid, kThreads, sm, st,
         (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
         q.s1, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s);
   }
@@ -564,12 +567,10 @@ cudaError_t launch_decode_combine(mla_dtype dt, const View3& o_lat, float* lse,
   (void)seq_lens;
   const dim3 grid(B, (H + 3) / 4);
   if (dt == MLA_F32)
-    decode_combine_kernel<float><<<grid, 128, 0, st>>>((float*)o_lat.data, o_lat.s0, o_lat.s1, lse,
-                                                       B, H, L, s);
-  else
-    decode_combine_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(
-        (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, B, H, L, s);
-  return cudaGetLastError();
+    return launch_k(decode_combine_kernel<float>, grid, 128, 0, st, (float*)o_lat.data, o_lat.s0, o_lat.s1, lse,
+                    B, H, L, s);
+  return launch_k(decode_combine_kernel<__nv_bfloat16>, grid, 128, 0, st, (__nv_bfloat16*)o_lat.data, o_lat.s0,
+                  o_lat.s1, lse, B, H, L, s);
 }
 
 cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
@@ -581,12 +582,12 @@ cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, co
   const size_t sm = simt_smem_bytes(L + R);
   if (dt == MLA_F32) {
     allow_smem(prefill_simt_kernel<float>, sm);
-    prefill_simt_kernel<float><<<grid, kThreads, sm, st>>>(
+    return launch_k(prefill_simt_kernel<float>, grid, kThreads, sm, st,
         (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
         block_table, bt_stride, max_blocks, cu_q, kv_lens, B, H, L, R, scale);
   } else {
     allow_smem(prefill_simt_kernel<__nv_bfloat16>, sm);
-    prefill_simt_kernel<__nv_bfloat16><<<grid, kThreads, sm, st>>>(
+    return launch_k(prefill_simt_kernel<__nv_bfloat16>, grid, kThreads, sm, st,
         (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
         q.s1, cache, block_table, bt_stride, max_blocks, cu_q, kv_lens, B, H, L, R, scale);
   }

@@ -336,6 +336,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync();   // barriers of both CTAs initialised before any remote access
   tc_fence_after();
+  pdl_enter();      // the queries, the cache and the schedule come from the kernels before
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort_flag;
 #ifdef MLA_TRACE
@@ -885,6 +886,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Row tiles per sequence (prefill), prefix-summed: one CTA.
 __global__ void prefill_items_kernel(const int32_t* __restrict__ cu_q, int B, int tpt, int32_t* __restrict__ out) {
+  pdl_enter();
   if (threadIdx.x == 0 && blockIdx.x == 0) {
     int acc = 0;
     for (int b = 0; b < B; ++b) {
@@ -962,8 +964,7 @@ cudaError_t launch_tc(const TcParams& p, const CUtensorMap& km, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(mla_attn_tc_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  mla_attn_tc_kernel<kRope><<<dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st>>>(km, rm, p);
-  return cudaGetLastError();
+  return launch_k(mla_attn_tc_kernel<kRope>, dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st, km, rm, p);
 }
 
 }  // namespace
@@ -1058,8 +1059,7 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
   p.cu_q = cu_q;
   p.kv_lens = kv_lens;
   p.item_prefix = item_prefix;
-  prefill_items_kernel<<<1, 32, 0, st>>>(cu_q, B, p.tpt, item_prefix);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(prefill_items_kernel, 1, 32, 0, st, cu_q, B, p.tpt, item_prefix);
   if (e != cudaSuccess) return e;
   const int clusters = R == 64 ? max_clusters<64>() : max_clusters<0>();
   return run_tc(MLA_BF16, p, q, cache, clusters, st);

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kThreads) bmm_simt_kernel(
     T* __restrict__ out, int64_t o_s0, int64_t o_s1, const T* __restrict__ a, int64_t a_s0,
     int64_t a_s1, const T* __restrict__ b, int64_t b_s0, int64_t b_s1, int M, int K, int N) {
   extern __shared__ float a_sm[];  // [kRows][K]
+  pdl_enter();
   const int g = blockIdx.y;
   const int m0 = blockIdx.z * kRows;
   const int n0 = blockIdx.x * kCols;
@@ -68,14 +69,13 @@ cudaError_t launch_bmm_simt(mla_dtype dt, const View3& out, const View3& a, cons
   if (dt == MLA_F32) {
     auto k = bmm_simt_kernel<float>;
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kThreads, smem, st>>>((float*)out.data, out.s0, out.s1, (const float*)a.data, a.s0,
-                                    a.s1, (const float*)b.data, b.s0, b.s1, M, K, N);
+    return launch_k(k, grid, kThreads, smem, st, (float*)out.data, out.s0, out.s1, (const float*)a.data, a.s0,
+                    a.s1, (const float*)b.data, b.s0, b.s1, M, K, N);
   } else {
     auto k = bmm_simt_kernel<__nv_bfloat16>;
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, kThreads, smem, st>>>((__nv_bfloat16*)out.data, out.s0, out.s1,
-                                    (const __nv_bfloat16*)a.data, a.s0, a.s1,
-                                    (const __nv_bfloat16*)b.data, b.s0, b.s1, M, K, N);
+    return launch_k(k, grid, kThreads, smem, st, (__nv_bfloat16*)out.data, out.s0, out.s1,
+                    (const __nv_bfloat16*)a.data, a.s0, a.s1, (const __nv_bfloat16*)b.data, b.s0, b.s1, M, K, N);
   }
   return cudaGetLastError();
 }

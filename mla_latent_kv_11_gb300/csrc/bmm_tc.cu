@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* abort = abort_flag;
+  pdl_enter();   // the operands may come from the kernel before: everything below reads them
 
   if (warp == 0 && lane == 0) {
     // producer
@@ -208,8 +209,7 @@ cudaError_t launch(const CUtensorMap& am, const CUtensorMap& bm, const CUtensorM
   cudaError_t e = cudaFuncSetAttribute(bmm_tc_kernel<kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const dim3 grid(N / kBN, (M + kBM - 1) / kBM, G);
-  bmm_tc_kernel<kBN><<<grid, kThreads, C::kSmem, st>>>(am, bm, cm, K);
-  return cudaGetLastError();
+  return launch_k(bmm_tc_kernel<kBN>, grid, kThreads, C::kSmem, st, am, bm, cm, K);
 }
 
 }  // namespace

@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(256) concat_q_kernel(
     W* __restrict__ out, int64_t o_s0, int64_t o_s1, const W* __restrict__ nope, int64_t n_s0,
     int64_t n_s1, const W* __restrict__ rope, int64_t r_s0, int64_t r_s1, int64_t H, int64_t Lw,
     int64_t Rw, int64_t total) {
+  pdl_enter();
   const int64_t Ew = Lw + Rw;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -49,6 +50,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     W* __restrict__ cache, int64_t c_blk, int64_t c_row, int64_t num_rows, int32_t page,
     const W* __restrict__ kv_c, int64_t k_s0, const W* __restrict__ k_pe, int64_t p_s0,
     const int64_t* __restrict__ slots, int64_t Lw, int64_t Rw, int64_t total) {
+  pdl_enter();
   const int64_t Ew = Lw + Rw;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -88,17 +90,17 @@ cudaError_t launch_concat_q(mla_dtype dt, const View3& out, const View3& nope, c
   const void* rp = R == 0 ? nope.data : rope.data;  // never read when R == 0
   if (vec) {
     const int64_t total = T * H * (L + R) / per;
-    concat_q_kernel<uint4><<<grid_for(total), 256, 0, st>>>(
+    return launch_k(concat_q_kernel<uint4>, grid_for(total), 256, 0, st,
         (uint4*)out.data, out.s0 / per, out.s1 / per, (const uint4*)nope.data, nope.s0 / per,
         nope.s1 / per, (const uint4*)rp, rope.s0 / per, rope.s1 / per, H, L / per, R / per, total);
   } else {
     const int64_t total = T * H * (L + R);
     if (es == 4)
-      concat_q_kernel<uint32_t><<<grid_for(total), 256, 0, st>>>(
+      return launch_k(concat_q_kernel<uint32_t>, grid_for(total), 256, 0, st,
           (uint32_t*)out.data, out.s0, out.s1, (const uint32_t*)nope.data, nope.s0, nope.s1,
           (const uint32_t*)rp, rope.s0, rope.s1, H, L, R, total);
     else
-      concat_q_kernel<uint16_t><<<grid_for(total), 256, 0, st>>>(
+      return launch_k(concat_q_kernel<uint16_t>, grid_for(total), 256, 0, st,
           (uint16_t*)out.data, out.s0, out.s1, (const uint16_t*)nope.data, nope.s0, nope.s1,
           (const uint16_t*)rp, rope.s0, rope.s1, H, L, R, total);
   }
@@ -118,17 +120,17 @@ cudaError_t launch_cache_write(mla_dtype dt, const View3& cache, const View3& kv
   const void* kp = R == 0 ? kv_c.data : k_pe.data;
   if (vec) {
     const int64_t total = T * (L + R) / per;
-    cache_write_kernel<uint4><<<grid_for(total), 256, 0, st>>>(
+    return launch_k(cache_write_kernel<uint4>, grid_for(total), 256, 0, st,
         (uint4*)cache.data, cache.s0 / per, cache.s1 / per, rows, page, (const uint4*)kv_c.data,
         kv_c.s0 / per, (const uint4*)kp, k_pe.s0 / per, slots, L / per, R / per, total);
   } else {
     const int64_t total = T * (L + R);
     if (es == 4)
-      cache_write_kernel<uint32_t><<<grid_for(total), 256, 0, st>>>(
+      return launch_k(cache_write_kernel<uint32_t>, grid_for(total), 256, 0, st,
           (uint32_t*)cache.data, cache.s0, cache.s1, rows, page, (const uint32_t*)kv_c.data,
           kv_c.s0, (const uint32_t*)kp, k_pe.s0, slots, L, R, total);
     else
-      cache_write_kernel<uint16_t><<<grid_for(total), 256, 0, st>>>(
+      return launch_k(cache_write_kernel<uint16_t>, grid_for(total), 256, 0, st,
           (uint16_t*)cache.data, cache.s0, cache.s1, rows, page, (const uint16_t*)kv_c.data,
           kv_c.s0, (const uint16_t*)kp, k_pe.s0, slots, L, R, total);
   }

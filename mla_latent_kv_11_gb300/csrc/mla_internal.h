@@ -2,6 +2,7 @@
 // Nothing here is part of the C ABI (include/mla.h is).
 #pragma once
 
+#include <utility>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -23,6 +24,35 @@ struct View3 {
   int64_t n0, n1, n2;
   int64_t s0, s1, s2;
 };
+
+// Programmatic dependent launch. Every kernel of the library is launched with programmatic
+// stream serialization, so its launch and prologue overlap the end of the kernel before it in
+// the stream. Each kernel calls pdl_enter() before it touches memory an earlier kernel may
+// write: griddepcontrol.wait returns once the preceding grid has completed and its writes are
+// visible (at once if the preceding stream work was not a programmatic launch), and
+// launch_dependents then lets the next kernel start launching.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 inline View3 view3(const mla_tensor& t) {
   return View3{t.data, t.shape[0], t.shape[1], t.shape[2], t.stride[0], t.stride[1], t.stride[2]};
