@@ -172,3 +172,49 @@ def test_decode_large_variable_lengths_sampled(mla):
                                    g.d_rope, w.scale, ids=ids)
     check_close(got[ids], want, "bf16", "large decode (sampled sequences)")
     check_lse(lse[ids], want_lse)
+
+
+def _ragged_batch(B, H, E, max_len, page, seed, dtype):
+    lens = (mi.randint(seed, B, 0, max_len + 1) * (mi.unit01(seed + 1, B) < 0.85)).astype(np.int64)
+    need = [(int(n) + page - 1) // page for n in lens]
+    nb = sum(need) + 1
+    perm = mi.permutation(seed + 2, nb)
+    table = np.zeros((B, max(max(need), 1)), np.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    cache = mi.encode(mi.draw("normal", seed + 3, nb * page * E, 0.5), dtype).reshape(nb, page, E)
+    q = mi.encode(mi.draw("normal", seed + 4, B * H * E, 0.5), dtype).reshape(B, H, E)
+    return [int(x) for x in lens], table, cache, q
+
+
+@pytest.mark.parametrize("splits", [0, 1100])
+def test_decode_schedule_beyond_shared_memory(mla, splits):
+    # 2100 sequences (the schedule keeps at most 2048 in shared memory) and, with 1100 splits,
+    # more work units than its shared unit array holds: both fall back to the workspace arrays.
+    H, L, R, page = 16, 512, 64, 16
+    E = L + R
+    lens, table, cache, q = _ragged_batch(2100, H, E, 80, page, 301, "bf16")
+    scale = 1.0 / math.sqrt(192)
+    o, lse = run_decode(mla, q, cache, table, lens, "bf16", L, R, scale, splits)
+    got = to_f64(o)
+    assert np.all(np.isfinite(got))
+    ids = [0, 1, 2, 1000, 2047, 2048, 2049, 2099] + [b for b in range(len(lens)) if lens[b] == 0][:2]
+    want, want_lse = oracle_decode(q, cache, table, lens, "bf16", L, R, scale, ids=ids)
+    check_close(got[ids], want, "bf16", f"2100 sequences, splits {splits}")
+    check_lse(lse[ids], want_lse, "bf16")
+
+
+def test_decode_v3_more_units_than_tiles(mla):
+    # The tensor-core path with 1100 work units for a batch of fewer tiles: most units get empty
+    # ranges, the unit boundaries live in the workspace, and the result must not change.
+    H, E, L, R = mi.V3.n_head, mi.V3.entry, mi.V3.kv_rank, mi.V3.d_rope
+    lens, table, cache, q = _ragged_batch(8, H, E, 1500, 64, 311, "bf16")
+    scale = 1.0 / math.sqrt(192)
+    o1, lse1 = run_decode(mla, q, cache, table, lens, "bf16", L, R, scale, 1100)
+    o0, lse0 = run_decode(mla, q, cache, table, lens, "bf16", L, R, scale, 0)
+    want, want_lse = oracle_decode(q, cache, table, lens, "bf16", L, R, scale)
+    check_close(to_f64(o1), want, "bf16", "v3 decode, 1100 units")
+    check_lse(lse1, want_lse, "bf16")
+    check_close(to_f64(o0), want, "bf16", "v3 decode, default units")
