@@ -19,27 +19,28 @@
 //   Q half [352, 480) latent, [480, 496) rope, bf16 pairs | l [496,512) fp32,
 // where l, the row sums of P, comes from an N=16 MMA of P against a tile of
 // ones issued with each PV (so the denominator sums exactly the bf16 P that O
-// accumulates, and the softmax warps never add P up),
-// so both MMAs take their A operand from TMEM and shared memory only streams
-// the B operand (the cache tile). The latent columns arrive in 64-column boxes
-// with 128-byte swizzle, the 32 rope columns in one box with 64-byte swizzle.
-// Shared memory holds 4 cache-tile stages (36 KB with rope, 32 KB without)
-// and two outgoing and two incoming exchange slots.
+// accumulates, and the softmax warps never add P up). Both MMAs take their A
+// operand from TMEM; shared memory only streams the B operand (the cache
+// tile): the latent columns in 64-column boxes with 128-byte swizzle, the 32
+// rope columns in one box with 64-byte swizzle. Shared memory holds 5 cache
+// stages (36 KB with rope, 32 KB without), the tile of ones, one outgoing
+// exchange tile (two pieces) and a ring of three incoming pieces: 226 KB.
 //
-// Exchange. The SM-to-SM network moves only about 10 bytes per clock each way,
-// so the pair does not swap fp32 partial scores (32 KB per tile) but
+// Exchange. The SM-to-SM network moves about 19 bytes per clock each way, so
+// the pair does not swap fp32 partial scores (32 KB per tile) but
 // exponentials: each CTA takes its row maximum of x_r = s_r * scale * log2 e,
-// rounded up to an integer c_r, and sends E_r = 2^(x_r - c_r) in bf16 with c_r
-// (16.5 KB per tile). Since
+// rounded up to an integer c_r, and sends E_r = 2^(x_r - c_r) in bf16 with c_r,
+// as two 8.5 KB pieces (keys 0..31 and 32..63): the first goes out as soon as
+// its 32 exponentials are written, while the second is computed. Since
 //   2^(x_0 + x_1 - m) = E_0 * E_1 * 2^(c_0 + c_1 - m),
-// both CTAs form the same P from the same bf16 operands in the same order;
-// c_0 + c_1 bounds the row maximum from above, so nothing can overflow, and
-// it is an integer, so every rescaling factor is an exact power of two: P is
-// E_0 * E_1 rounded once to bf16 (the PV MMA takes bf16 anyway). A
-// dedicated exchange warpgroup reads S out of TMEM as soon as the MMA has
-// produced it, computes c and E and pushes them with one bulk copy (completion
-// counted in bytes on the peer's barrier); the softmax warpgroup combines the
-// two halves concurrently.
+// both CTAs form P = bf16(E_own * E_peer) * 2^(M - m), the same value in both
+// (IEEE multiplication commutes); c_0 + c_1 bounds the row maximum from
+// above, so nothing can overflow, and it is an integer, so every rescaling
+// factor is an exact power of two. A dedicated exchange warpgroup reads S out
+// of TMEM as soon as the MMA has produced it, computes c and E and pushes each
+// piece with one bulk copy into the peer's incoming ring (completion counted in
+// bytes on the peer's barrier); the softmax warpgroup takes its own tile at
+// once and each peer piece as it lands.
 //
 // Roles (384 threads): warp 0 issues TMA loads, warp 1 issues MMAs (a polling
 // state machine that issues whichever of QK(g+1) and PV(g) is ready; the warp
@@ -48,12 +49,11 @@
 // owns the TMEM allocation, warps 4..7 load Q into TMEM and run the exchange,
 // warps 8..11 run the softmax, the O rescale and the epilogue, one thread per
 // query row (TMEM lane) in each group; warp 3 forwards the softmax group's
-// "incoming buffer read" signals to the peer (a cluster-scope release stalls
-// the issuing thread for about a microsecond, so it is kept off the softmax).
-// Every wait is bounded in time; a timeout winds the kernel down and reports
-// MLA_ERR_TIMEOUT instead of hanging.
+// "incoming piece read" signals to the peer as relaxed remote arrives (the
+// reads they answer for were completed by a bar.sync). Every wait is bounded
+// in time; a timeout winds the kernel down and reports MLA_ERR_TIMEOUT
+// instead of hanging.
 //
-
 // The running reference maximum m is updated lazily: O and its denominator are
 // rescaled only when the bound c_0 + c_1 exceeds m by more than 8, so P stays
 // below 2^8.
@@ -636,38 +636,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 2^(M - m) of the softmax an exact power of two
         c = c == -CUDART_INF_F ? -CUDART_INF_F : ceilf(c * p.scale_log2);
         const float neg_c = c == -CUDART_INF_F ? 0.f : -c;
-        uint32_t ek[32];
-#pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(ex2_approx(fmaf(sv[k], p.scale_log2, neg_c)),
-                                                         ex2_approx(fmaf(sv[k + 1], p.scale_log2, neg_c)));
-          ek[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        // ---- both pieces into the outgoing slot (row r's 64 bytes of a piece as four 16-byte
-        // chunks, rotated by (r / 2) % 4 against bank conflicts), then each piece to the peer
+        // ---- each half: E of its 32 keys into its piece, then straight to the peer, so the
+        // first piece is on its way while the second is computed
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          uint32_t ek[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(ex2_approx(fmaf(sv[32 * h + k], p.scale_log2, neg_c)),
+                                                            ex2_approx(fmaf(sv[32 * h + k + 1], p.scale_log2, neg_c)));
+            ek[k >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
           unsigned char* piece = sXloc + h * kXSlot;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
             *reinterpret_cast<uint4*>(piece + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4)) =
-                make_uint4(ek[16 * h + 4 * ch], ek[16 * h + 4 * ch + 1], ek[16 * h + 4 * ch + 2],
-                           ek[16 * h + 4 * ch + 3]);
+                make_uint4(ek[4 * ch], ek[4 * ch + 1], ek[4 * ch + 2], ek[4 * ch + 3]);
           reinterpret_cast<float*>(piece + kESlotBytes)[row] = c;
-        }
-        fence_proxy_async_smem();
-        named_bar(kXchgBar, 128);
-        MLA_TRACE_AT(4, t);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.own_ready);
-        if (row == 0) {
-          for (int h = 0; sent && h < 2; ++h) {
+          fence_proxy_async_smem();
+          named_bar(kXchgBar, 128);
+          if (h == 1) {
+            MLA_TRACE_AT(4, t);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.own_ready);
+          }
+          if (row == 0 && sent) {
             // piece q goes to the peer's incoming slot q % 3, free once it has read piece q - 3
             const int q = 2 * t + h, rs = q % kInSlots;
             sent = mbar_wait<true>(&bars.x_empty[rs], ((q / kInSlots) & 1) ^ 1, abort);
             if (h == 0) MLA_TRACE2_AT(0, t);
             if (sent) {
-              bulk_copy_to_peer(peer_rem0 + rs * kXSlot, sXloc + h * kXSlot, kXSlot, peer_xfull0 + rs * 8);
+              bulk_copy_to_peer(peer_rem0 + rs * kXSlot, piece, kXSlot, peer_xfull0 + rs * 8);
               bulk_commit_group();
             }
           }
