@@ -458,9 +458,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t spins = 0;
       while (ok && pv < nt) {
         bool did = false;
-        if (qk < nt) {
+        if (qk < nt && qk <= pv + 2) {
           const int t = gt + qk, s = t % C::kStages;
-          // S is single-buffered: QK(t) needs S(t-1) read out by the exchange group
+          // S is single-buffered: QK(t) needs S(t-1) read out by the exchange group. At most two
+          // QKs run ahead of the PVs: a third would hold up PV(t) behind its issue (measured)
           if (uni(mbar_poll(&bars.kv_full[s], (t / C::kStages) & 1) && mbar_poll(&bars.s_empty, (t & 1) ^ 1))) {
             MLA_TRACE_AT(1, t);
             tc_fence_after();
