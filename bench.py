@@ -181,8 +181,9 @@ class DecodeStep:
         self.launches_per_step = 7
 
     def run(self, ev_decode=None, q_nope=None, q_pe=None, kv_c=None, k_pe=None, slots=None,
-            table=None, lens=None):
+            table=None, lens=None, out=None):
         m = self.mla
+        out = self.out if out is None else out
         q_nope = self.q_nope if q_nope is None else q_nope
         m.mla_absorb_q(self.q_lat, q_nope.transpose(0, 1), self.w_uk)
         m.mla_concat_q(self.q_cat, self.q_lat.transpose(0, 1), self.q_pe if q_pe is None else q_pe)
@@ -194,7 +195,7 @@ class DecodeStep:
                      self.lens if lens is None else lens, self.L, self.R, self.w.scale, workspace=self.ws)
         if ev_decode is not None:
             ev_decode[1].record()
-        m.mla_v_up(self.out.transpose(0, 1), self.o_lat.transpose(0, 1), self.w_uv)
+        m.mla_v_up(out.transpose(0, 1), self.o_lat.transpose(0, 1), self.w_uv)
 
 
 def _smi_id(local: int) -> str:
@@ -401,34 +402,63 @@ def run_ours(args) -> None:
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     clocks = clk.summary()
 
-    # end to end through the same calls with host buffers: pinned H2D of the step's inputs,
-    # the five calls, D2H of the output
+    # end to end through the same calls with host buffers: every step copies its inputs in from
+    # pinned host memory, runs the five calls and copies its output back; like a serving loop,
+    # the copies of neighbouring steps run on two copy streams under the compute (two sets of
+    # device buffers, ordered by events), and the timed region ends when the last output is back
     def pinned(t):
         return t.detach().cpu().pin_memory()
 
-    host = {k: pinned(getattr(step, k)) for k in ("q_nope", "q_pe", "new_kv_c", "new_k_pe", "slots",
-                                                    "table", "lens")}
-    dev_in = {k: torch.empty_like(getattr(step, k)) for k in host}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    names = ("q_nope", "q_pe", "new_kv_c", "new_k_pe", "slots", "table", "lens")
+    host = {k: pinned(getattr(step, k)) for k in names}
+    dev_in = [{k: torch.empty_like(getattr(step, k)) for k in names} for _ in range(2)]
+    dev_out = [torch.empty_like(step.out) for _ in range(2)]
+    out_host = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
 
-    def e2e_step():
-        for k, t in host.items():
-            dev_in[k].copy_(t, non_blocking=True)
-        step.run(**{"q_nope": dev_in["q_nope"], "q_pe": dev_in["q_pe"], "kv_c": dev_in["new_kv_c"],
-                    "k_pe": dev_in["new_k_pe"], "slots": dev_in["slots"], "table": dev_in["table"],
-                    "lens": dev_in["lens"]})
-        out_host.copy_(step.out, non_blocking=True)
+    def h2d_copy(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["done"][b])        # step i-2 has finished reading these buffers
+            for k in names:
+                dev_in[b][k].copy_(host[k], non_blocking=True)
+            ev["in"][b].record(s_in)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def e2e_run(i):
+        b = i % 2
+        stream.wait_event(ev["in"][b])
+        if i >= 2:
+            stream.wait_event(ev["out"][b])           # step i-2's output has left this buffer
+        d = dev_in[b]
+        step.run(q_nope=d["q_nope"], q_pe=d["q_pe"], kv_c=d["new_kv_c"], k_pe=d["new_k_pe"],
+                 slots=d["slots"], table=d["table"], lens=d["lens"], out=dev_out[b])
+        ev["done"][b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["done"][b])
+            out_host[b].copy_(dev_out[b], non_blocking=True)
+            ev["out"][b].record(s_out)
+
+    def e2e_loop(n):
+        s_in.wait_stream(stream)      # the copies start after everything queued so far (the
+        s_out.wait_stream(stream)     # timing event included)
+        h2d_copy(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d_copy(i + 1)
+            e2e_run(i)
+        stream.wait_stream(s_out)
+        stream.wait_stream(s_in)
+
+    e2e_loop(args.warmup)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_loop(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
