@@ -179,16 +179,27 @@ class DecodeStep:
         self.out = torch.empty((B, H, V), dtype=dt, device=device)
         self.ws = torch.empty(mla.mla_decode_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
         self.launches_per_step = 7
+        # the cache write does not depend on the query path (absorb, concat): it runs on a side
+        # stream concurrently with it and joins before the decode
+        self.side = torch.cuda.Stream(device)
+        self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
 
     def run(self, ev_decode=None, q_nope=None, q_pe=None, kv_c=None, k_pe=None, slots=None,
             table=None, lens=None, out=None):
+        import torch
         m = self.mla
         out = self.out if out is None else out
         q_nope = self.q_nope if q_nope is None else q_nope
+        main = torch.cuda.current_stream()
+        self.ev_fork.record(main)
+        self.side.wait_event(self.ev_fork)
+        with torch.cuda.stream(self.side):
+            m.mla_cache_write(self.cache, self.new_kv_c if kv_c is None else kv_c,
+                              self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
+            self.ev_join.record(self.side)
         m.mla_absorb_q(self.q_lat, q_nope.transpose(0, 1), self.w_uk)
         m.mla_concat_q(self.q_cat, self.q_lat.transpose(0, 1), self.q_pe if q_pe is None else q_pe)
-        m.mla_cache_write(self.cache, self.new_kv_c if kv_c is None else kv_c,
-                          self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
+        main.wait_event(self.ev_join)
         if ev_decode is not None:
             ev_decode[0].record()
         m.mla_decode(self.o_lat, self.q_cat, self.cache, self.table if table is None else table,
