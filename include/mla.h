@@ -212,6 +212,17 @@ mla_status mla_decode_noalloc(mla_dtype dtype, mla_tensor o_lat_out, float* lse_
  * bounded wait that gave up: MLA_ERR_TIMEOUT). MLA_OK if none was set. */
 mla_status mla_device_error(void* stream);
 
+/* Self-check of failure detection. Every wait in the library's kernels is
+ * bounded in time: a wait that gives up records MLA_ERR_TIMEOUT for
+ * mla_device_error and the kernel winds down, so a stuck pipeline never hangs
+ * the GPU. This call launches one warp that runs that same bounded wait on an
+ * mbarrier nothing ever arrives on, with a limit of limit_us microseconds
+ * (1 .. 1000000) instead of the kernels' 2 s; afterwards mla_device_error on
+ * the same stream reports MLA_ERR_TIMEOUT (and clears it) while the context
+ * stays usable. Returns MLA_ERR_INVALID_ARG for a limit out of range. The
+ * source pages have no counterpart of this call. */
+mla_status mla_check_bounded_wait(uint32_t limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

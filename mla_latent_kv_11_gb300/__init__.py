@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
             "mla_decode_noalloc": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, I32, P],
                                    ctypes.c_int),
             "mla_device_error": ([P], ctypes.c_int),
+            "mla_check_bounded_wait": ([ctypes.c_uint32, P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(h, name)
@@ -227,6 +228,11 @@ def mla_decode_noalloc(o_lat_out, q_cat, cache, block_table, seq_lens, kv_lora_r
                                     block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
                                     seq_lens.data_ptr(), kv_lora_rank, rope_dim, softmax_scale,
                                     num_splits, _stream(stream)))
+
+
+def mla_check_bounded_wait(limit_us: int, stream=None) -> None:
+    """Run the kernels' bounded wait on an mbarrier nothing arrives on (see include/mla.h)."""
+    _check(lib().mla_check_bounded_wait(limit_us, _stream(stream)))
 
 
 def mla_device_error(stream=None) -> None:

@@ -240,6 +240,28 @@ cudaError_t launch_bmm_tc(const View3& out, const View3& a, const View3& b, cuda
   return bn == 256 ? launch<256>(am, bm, cm, G, M, N, K, st) : launch<128>(am, bm, cm, G, M, N, K, st);
 }
 
+namespace {
+// One warp waits, with the bounded wait every kernel of the library uses, on an mbarrier that
+// nothing arrives on; when the wait gives up it records kErrTimeout like any kernel would.
+__global__ void wait_check_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  pdl_enter();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0, &abort_flag, limit_ns);
+  if (!ok && threadIdx.x == 0) atomicOr(&g_bmm_err, kErrTimeout);
+}
+}  // namespace
+
+cudaError_t launch_wait_check(uint32_t limit_us, cudaStream_t st) {
+  return launch_k(wait_check_kernel, 1, 32, 0, st, (uint64_t)limit_us * 1000ull);
+}
+
 unsigned bmm_tc_errors_read_clear() {
   unsigned v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_bmm_err, sizeof(v)) != cudaSuccess) return 0;

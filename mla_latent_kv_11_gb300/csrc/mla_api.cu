@@ -370,6 +370,13 @@ mla_status mla_prefill(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, ml
                      "mla_prefill");
 }
 
+mla_status mla_check_bounded_wait(uint32_t limit_us, void* stream) {
+  g_msg[0] = 0;
+  if (limit_us == 0 || limit_us > 1000000u)
+    return fail(MLA_ERR_INVALID_ARG, "limit_us must be in [1, 1000000], got %u", limit_us);
+  return cuda_status(launch_wait_check(limit_us, (cudaStream_t)stream), "mla_check_bounded_wait");
+}
+
 mla_status mla_device_error(void* stream) {
   g_msg[0] = 0;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

@@ -139,5 +139,6 @@ unsigned copy_errors_read_clear();
 unsigned attn_simt_errors_read_clear();
 unsigned attn_tc_errors_read_clear();
 unsigned bmm_tc_errors_read_clear();
+cudaError_t launch_wait_check(uint32_t limit_us, cudaStream_t st);
 
 }  // namespace mla

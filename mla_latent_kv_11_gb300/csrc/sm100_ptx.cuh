@@ -100,14 +100,15 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitim
 // Wait for phase `parity` of `bar` to complete. Returns false (and sets *abort)
 // if the wait ran out of time or another thread already aborted.
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }

@@ -107,3 +107,11 @@ def test_decode_and_prefill_validation(mla):
     assert lib.mla_prefill(1, o, None, q, cache, 0x2000, 4, 4, None, 0x3000, 2, 1, L, R, 0.1, None, 0,
                            None) == mla.MLA_ERR_INVALID_ARG         # null cu_seqlens_q
     del ok_args
+
+
+def test_bounded_wait_check_rejects_bad_limits_without_a_launch(mla):
+    # checked on the host before anything reaches the device (stream 0 needs no GPU here)
+    for limit in (0, 1_000_001):
+        with pytest.raises(mla.MlaError) as e:
+            mla.mla_check_bounded_wait(limit, stream=0)
+        assert e.value.status == mla.MLA_ERR_INVALID_ARG
