@@ -173,7 +173,6 @@ class DecodeStep:
         self.lens = torch.from_numpy(w.seq_lens).to(device)
         self.cache = dev(w.full_cache())
         B, H, L, E, V = self.B, self.H, self.L, self.E, self.V
-        self.q_lat = torch.empty((H, B, L), dtype=dt, device=device)
         self.q_cat = torch.empty((B, H, E), dtype=dt, device=device)
         self.o_lat = torch.empty((B, H, L), dtype=dt, device=device)
         self.out = torch.empty((B, H, V), dtype=dt, device=device)
@@ -197,8 +196,11 @@ class DecodeStep:
             m.mla_cache_write(self.cache, self.new_kv_c if kv_c is None else kv_c,
                               self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
             self.ev_join.record(self.side)
-        m.mla_absorb_q(self.q_lat, q_nope.transpose(0, 1), self.w_uk)
-        m.mla_concat_q(self.q_cat, self.q_lat.transpose(0, 1), self.q_pe if q_pe is None else q_pe)
+        # the absorb writes q_lat straight into q_cat's first L columns (a [H,B,L] view of it),
+        # so the concat finds its nope operand in place and copies only the rope columns
+        lat = self.q_cat[:, :, :self.L]
+        m.mla_absorb_q(lat.transpose(0, 1), q_nope.transpose(0, 1), self.w_uk)
+        m.mla_concat_q(self.q_cat, lat, self.q_pe if q_pe is None else q_pe)
         main.wait_event(self.ev_join)
         if ev_decode is not None:
             ev_decode[0].record()

@@ -105,7 +105,11 @@ mla_status mla_absorb_q(mla_dtype dtype, mla_tensor q_lat_out, mla_tensor q_nope
  * is broadcast to every head, as for _concat_k_nope_k_pe).
  *   q_cat_out [T,H,L+R] (written), nope [T,H,L], rope [T,H,R] or [T,1,R]
  *   (a rope stride(1) of 0 also broadcasts). Bits are copied unchanged,
- *   including NaN payloads and signed zeros. R may be 0. */
+ *   including NaN payloads and signed zeros. R may be 0.
+ *   nope may be q_cat_out's own first L columns (the same data pointer and
+ *   strides: mla_absorb_q can write q_lat straight into q_cat_out); then only
+ *   the rope columns are copied. Any other overlap of q_cat_out with an input
+ *   is undefined. */
 mla_status mla_concat_q(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope,
                         mla_tensor rope, void* stream);
 

@@ -228,8 +228,18 @@ mla_status mla_concat_q(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope, 
   View3 r = view3(rope);
   if (rope.shape[1] == 1) r.s1 = 0;  // one rope head broadcast to every head
   r.n1 = H;
-  return cuda_status(launch_concat_q(dtype, view3(q_cat_out), view3(nope), r, (cudaStream_t)stream),
-                     "mla_concat_q");
+  View3 out = view3(q_cat_out), nv = view3(nope);
+  if (nope.data == q_cat_out.data && nope.stride[0] == q_cat_out.stride[0] &&
+      nope.stride[1] == q_cat_out.stride[1] && nope.stride[2] == q_cat_out.stride[2]) {
+    // nope is q_cat_out's own first L columns (the absorb wrote q_lat in place): they are
+    // already there, only the rope columns move
+    const size_t es = dtype == MLA_F32 ? 4 : 2;
+    out.data = static_cast<char*>(out.data) + es * (size_t)nope.shape[2];
+    out.n2 = rope.shape[2];
+    nv.n2 = 0;
+    if (rope.shape[2] == 0) return MLA_OK;
+  }
+  return cuda_status(launch_concat_q(dtype, out, nv, r, (cudaStream_t)stream), "mla_concat_q");
 }
 
 mla_status mla_cache_write(mla_dtype dtype, mla_tensor cache, mla_tensor kv_c, mla_tensor k_pe,

@@ -123,3 +123,42 @@ def test_cache_write_padding_odd_widths_and_out_of_range(mla, dtype):
 
 def test_poison_constant_is_the_pages():
     assert BF16_POISON == 0x7FC0
+
+
+FUSED_CASES = [  # heads, batch, K (nope width), L, R, rope heads
+    (128, 64, 128, 512, 64, 128),   # V3 decode batch 64 (tensor-core bmm)
+    (16, 5, 128, 512, 64, 1),       # V2-Lite, one rope head broadcast
+    (3, 7, 12, 20, 3, 3),           # odd widths (SIMT bmm, element concat)
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", FUSED_CASES, ids=["v3_b64", "v2lite_bcast", "odd"])
+def test_absorb_into_q_cat_then_concat_in_place(mla, dtype, case):
+    # The absorb writes q_lat straight into q_cat's first L columns through a [H,B,L] view;
+    # the concat then gets those columns as its nope operand and moves only the rope.
+    import math
+    import torch
+    from helpers import check_close, to_f64
+    H, B, K, L, R, Hr = case
+    qn = mi.encode(mi.draw("uniform", 71, B * H * K), dtype).reshape(B, H, K)
+    w = mi.encode(mi.draw("uniform", 72, H * K * L, 1.0 / math.sqrt(K)), dtype).reshape(H, K, L)
+    rope = _bits(mi.normal(73, B * Hr * R), dtype).reshape(B, Hr, R)
+    q_cat = poisoned((B, H, L + R), dtype)
+    lat = q_cat[:, :, :L]
+    mla.mla_absorb_q(lat.transpose(0, 1), to_dev(qn, dtype).transpose(0, 1), to_dev(w, dtype))
+    mla.mla_concat_q(q_cat, lat, to_dev(rope, dtype))
+    torch.cuda.synchronize()
+    got_bits = to_host_bits(q_cat)
+    qn64 = np.transpose(mi.decode_f64(qn, dtype), (1, 0, 2))                # [H,B,K]
+    want_lat = np.transpose(orc.bmm(qn64, mi.decode_f64(w, dtype)), (1, 0, 2))  # [B,H,L]
+    check_close(to_f64(q_cat)[:, :, :L], want_lat, dtype, "absorbed latent columns")
+    # the rope columns are the oracle's concat of them, bit for bit
+    want_rope = orc.concat_q(got_bits[:, :, :L], rope)[:, :, L:]
+    assert np.array_equal(got_bits[:, :, L:].view(np.uint16 if dtype == "bf16" else np.uint32),
+                          want_rope.view(np.uint16 if dtype == "bf16" else np.uint32))
+    # the latent columns are what the same absorb writes into a buffer of its own
+    sep = poisoned((H, B, L), dtype)
+    mla.mla_absorb_q(sep, to_dev(qn, dtype).transpose(0, 1), to_dev(w, dtype))
+    torch.cuda.synchronize()
+    assert np.array_equal(np.transpose(to_host_bits(sep), (1, 0, 2)), got_bits[:, :, :L])
