@@ -133,14 +133,23 @@ struct Bars {
 // Cycle stamps of pipeline events of work unit 0, for tuning builds only.
 __device__ long long g_trace[2][8][512];
 __device__ long long g_trace2[2][8][512];
-__device__ long long g_cta_time[512][4];   // per CTA: SM id, start, end (globaltimer ns), tiles
-#define MLA_TRACE_AT(ev, g)                                              \
-  do {                                                                    \
-    if (unit == 0 && (g) < 512) g_trace[rank][ev][(g)] = clock64();      \
+// per CTA: SM id, start and end (globaltimer ns), tiles issued, start and end (clock64), cycles
+// the MMA issuer had a QK allowed but waited only on the cache tile, and only on S being free,
+// cycles spent issuing QK MMAs and PV MMAs
+__device__ long long g_cta_time[512][10];
+// the same stamps for every CTA, first 128 tiles of each
+__device__ long long g_trace_all[2][304][8][128];
+#define MLA_TRACE_AT(ev, g)                                                          \
+  do {                                                                                \
+    const long long now_ = clock64();                                                 \
+    if (unit == 0 && (g) < 512) g_trace[rank][ev][(g)] = now_;                        \
+    if (blockIdx.x < 304 && (g) < 128) g_trace_all[0][blockIdx.x][ev][(g)] = now_;    \
   } while (0)
-#define MLA_TRACE2_AT(ev, g)                                                          \
-  do {                                                                                 \
-    if (unit == 0 && row == 0 && (g) < 512) g_trace2[rank][ev][(g)] = clock64();      \
+#define MLA_TRACE2_AT(ev, g)                                                                  \
+  do {                                                                                         \
+    const long long now_ = clock64();                                                          \
+    if (unit == 0 && row == 0 && (g) < 512) g_trace2[rank][ev][(g)] = now_;                    \
+    if (row == 0 && blockIdx.x < 304 && (g) < 128) g_trace_all[1][blockIdx.x][ev][(g)] = now_; \
   } while (0)
 #else
 #define MLA_TRACE_AT(ev, g) \
@@ -345,6 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     g_cta_time[blockIdx.x][0] = smid;
     g_cta_time[blockIdx.x][1] = (long long)globaltimer_ns();
+    g_cta_time[blockIdx.x][4] = clock64();
   }
 #endif
 
@@ -439,6 +449,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_sum = idesc_bf16(kRows, 16, false, false);
     const uint32_t kv_base = smem_u32(sKV);
     const uint32_t ones_base = smem_u32(smem + C::kOffOnes);
+#ifdef MLA_TRACE
+    long long tr_starve = 0, tr_sblock = 0, tr_t0 = 0, tr_qkiss = 0, tr_pviss = 0, tr_i0 = 0;
+    int tr_state = 0;   // 0 none, 1 waiting on the tile only, 2 waiting on S only
+#endif
     while (ok && wk.next(p, sg)) {
       const int nt = ntiles(sg);
       if (nt == 0) {
@@ -462,8 +476,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int t = gt + qk, s = t % C::kStages;
           // S is single-buffered: QK(t) needs S(t-1) read out by the exchange group. At most two
           // QKs run ahead of the PVs: a third would hold up PV(t) behind its issue (measured)
-          if (uni(mbar_poll(&bars.kv_full[s], (t / C::kStages) & 1) && mbar_poll(&bars.s_empty, (t & 1) ^ 1))) {
+          const bool kv_ok = mbar_poll(&bars.kv_full[s], (t / C::kStages) & 1);
+          const bool s_ok = mbar_poll(&bars.s_empty, (t & 1) ^ 1);
+#ifdef MLA_TRACE
+          {
+            const int st = (kv_ok && s_ok) ? 0 : (!kv_ok && s_ok) ? 1 : (kv_ok && !s_ok) ? 2 : 3;
+            if (st != tr_state) {
+              const long long now = clock64();
+              if (tr_state == 1) tr_starve += now - tr_t0;
+              if (tr_state == 2) tr_sblock += now - tr_t0;
+              tr_state = st;
+              tr_t0 = now;
+            }
+          }
+#endif
+          if (uni(kv_ok && s_ok)) {
             MLA_TRACE_AT(1, t);
+#ifdef MLA_TRACE
+            tr_i0 = clock64();
+#endif
             tc_fence_after();
             const uint32_t kb = kv_base + s * C::kStageBytes;
 #pragma unroll
@@ -479,15 +510,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                    sdesc_sw64(kb + 4 * kBoxBytesK + kk * 32, 16, 512), id_qk, 1u);
             }
             umma_commit_elect(&bars.s_full);
+#ifdef MLA_TRACE
+            tr_qkiss += clock64() - tr_i0;
+#endif
             ++qk;
             did = true;
           }
         }
+#ifdef MLA_TRACE
+        else if (tr_state != 0) {
+          const long long now = clock64();
+          if (tr_state == 1) tr_starve += now - tr_t0;
+          if (tr_state == 2) tr_sblock += now - tr_t0;
+          tr_state = 0;
+        }
+#endif
         if (pv < qk) {
           const int t = gt + pv, s = t % C::kStages;
           const bool o_free = pv > 0 || seg_i == 0 || mbar_poll(&bars.o_empty, (seg_i - 1) & 1);
           if (uni(o_free && mbar_poll(&bars.p_full, t & 1))) {
             MLA_TRACE_AT(2, t);
+#ifdef MLA_TRACE
+            tr_i0 = clock64();
+#endif
             tc_fence_after();
             const uint32_t vb = kv_base + s * C::kStageBytes;
 #pragma unroll
@@ -502,6 +547,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma_commit_elect(&bars.kv_empty[s]);
             umma_commit_elect(&bars.pv_done);
             if (pv == nt - 1) umma_commit_elect(&bars.seg_done);
+#ifdef MLA_TRACE
+            tr_pviss += clock64() - tr_i0;
+#endif
             ++pv;
             did = true;
           }
@@ -521,6 +569,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++full_i;
     }
     if (!ok && lane == 0) set_abort(bars, peer);
+#ifdef MLA_TRACE
+    if (lane == 0 && blockIdx.x < 512) {
+      g_cta_time[blockIdx.x][3] = gt;
+      g_cta_time[blockIdx.x][6] = tr_starve;
+      g_cta_time[blockIdx.x][7] = tr_sblock;
+      g_cta_time[blockIdx.x][8] = tr_qkiss;
+      g_cta_time[blockIdx.x][9] = tr_pviss;
+    }
+#endif
     __syncwarp();
     // every MMA this warp issued is complete before the TMEM is released
     umma_commit_elect(&bars.mma_final);
@@ -875,7 +932,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (tid == 0 && bars.abort_flag) atomicOr(&g_tc_err, kErrTimeout);
 #ifdef MLA_TRACE
-  if (tid == 0 && blockIdx.x < 512) g_cta_time[blockIdx.x][2] = (long long)globaltimer_ns();
+  if (tid == 0 && blockIdx.x < 512) {
+    g_cta_time[blockIdx.x][2] = (long long)globaltimer_ns();
+    g_cta_time[blockIdx.x][5] = clock64();
+  }
 #endif
   if (warp == 2) {
     tc_fence_after();
@@ -1070,6 +1130,7 @@ extern "C" int mla_debug_trace(long long* host) {
   int e = (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
   if (!e) e = (int)cudaMemcpyFromSymbol(host + 2 * 8 * 512, g_trace2, sizeof(g_trace2));
   if (!e) e = (int)cudaMemcpyFromSymbol(host + 4 * 8 * 512, g_cta_time, sizeof(g_cta_time));
+  if (!e) e = (int)cudaMemcpyFromSymbol(host + 4 * 8 * 512 + 512 * 10, g_trace_all, sizeof(g_trace_all));
   return e;
 }
 #endif
