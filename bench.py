@@ -519,7 +519,8 @@ def run_ours(args) -> None:
 
 
 def component_figures(mla, mi, device) -> dict:
-    """Per-stage figures on the other workloads: prefill TFLOP/s, concat and cache-write GB/s."""
+    """Per-stage figures on the other workloads: prefill TFLOP/s, decode at a fixed 8192
+    context, concat and cache-write GB/s."""
     import numpy as np
     import torch
     out = {}
@@ -556,6 +557,22 @@ def component_figures(mla, mi, device) -> dict:
     out["prefill_nope_h64_4x2048"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
                                       "frac_of_bf16_peak": flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12)}
     del q, cache, o
+    # decode at a fixed 8192-token context: 64 sequences, 128 heads, page 64, a seeded block
+    # permutation (the "batch 64 x 8K context" reading of the large decode)
+    B, H, L, R, page, ctx = 64, 128, 512, 64, 64, 8192
+    E, nbl = L + R, ctx // page
+    cache = torch.randn((B * nbl, page, E), device=device, dtype=torch.bfloat16) * 0.1
+    table = torch.from_numpy(mi.permutation(8192, B * nbl).astype(np.int32).reshape(B, nbl)).to(device)
+    lens = torch.full((B,), ctx, dtype=torch.int32, device=device)
+    q = torch.randn((B, H, E), device=device, dtype=torch.bfloat16) * 0.1
+    o = torch.empty((B, H, L), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(mla.mla_decode_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
+    ms = timed(lambda: mla.mla_decode(o, q, cache, table, lens, L, R, 1.0 / math.sqrt(192), workspace=ws), reps=20)
+    nbytes = decode_algorithmic_bytes([ctx] * B, B, H, L, R, nbl)
+    out["decode_b64_ctx8192_fixed"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                                       "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                       "queries_per_s": B / (ms * 1e-3)}
+    del cache, table, q, o, ws
     # concat and cache write, unified-slot workload
     w = mi.write_concat_workload()
     Nh, Bq, Lq = w.q_nope_storage.shape
