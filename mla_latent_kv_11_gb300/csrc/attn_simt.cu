@@ -21,6 +21,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "mla_internal.h"
 
 namespace mla {
@@ -38,7 +40,7 @@ __device__ __forceinline__ void st(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // ---------------------------------------------------------------------------
-// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, at most 1024).
 __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -47,10 +49,11 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
+  const int nwarps = blockDim.x >> 5;
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_tot[lane];
+    int w = lane < nwarps ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
@@ -60,7 +63,7 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   }
   __syncthreads();
   const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
-  *total = warp_tot[31];
+  *total = warp_tot[nwarps - 1];
   __syncthreads();
   return before;
 }
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   }
   __syncthreads();
   // pass 1: tile prefix
-  for (int base = 0; base < B; base += 1024) {
+  for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     const int n = b < B ? (clamp_len(seq_lens, b, cap) + kTile - 1) / kTile : 0;
     int tot;
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   __syncthreads();
   const int total = carry_sh;
   // the number of sequences with tiles before each b
-  for (int base = 0; base < B; base += 1024) {
+  for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     const int nz = b < B && pre[b + 1] > pre[b] ? 1 : 0;
     int tot;
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   if (threadIdx.x == 0) carry_sh = 0;
   __syncthreads();
   // pass 2: units touching each sequence, and partial-slot bases
-  for (int base = 0; base < B; base += 1024) {
+  for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int np = 0, fu = 0;
     if (b < B) {
@@ -535,7 +538,11 @@ void allow_smem(K k, size_t bytes) {
 cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
                                    int32_t page, const DecodeSched& s, cudaStream_t st) {
   const long long cap = (long long)max_blocks * page;
-  return launch_k(decode_schedule_kernel, 1, 1024, 0, st, seq_lens, B, (int)(cap > INT32_MAX ? INT32_MAX : cap), s);
+  // one thread per sequence or unit boundary, in whole warps: a small batch waits on few warps
+  // at each of the kernel's barriers
+  const int need = (int)std::max<int64_t>(B, (int64_t)s.units + 1);
+  const int threads = std::min(1024, std::max(32, (need + 31) / 32 * 32));
+  return launch_k(decode_schedule_kernel, 1, threads, 0, st, seq_lens, B, (int)(cap > INT32_MAX ? INT32_MAX : cap), s);
 }
 
 cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
