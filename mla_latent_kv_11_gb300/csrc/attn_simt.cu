@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (h >= H) return;
   const int np = s.npieces[b];
+  const int base = s.piece_base[b];   // loaded beside np: one memory latency for both
   if (np == 1) return;
   T* o = o_lat + (int64_t)b * o_s0 + (int64_t)h * o_s1;
   if (np == 0) {
@@ -412,9 +413,53 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
     if (lane == 0 && lse_out) lse_out[(int64_t)b * H + h] = -CUDART_INF_F;
     return;
   }
-  const int base = s.piece_base[b];
   const float* lse_p = s.part_lse + (int64_t)base * H + h;
   const int64_t pstride = (int64_t)H * L;
+  const bool vec = (L % 4 == 0) && ((o_s0 | o_s1) % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(o_lat) % (4 * sizeof(T)) == 0);
+  if (vec && L == 512 && np <= 4) {
+    // up to four pieces: their maxima and their rows are loaded together, so the warp waits
+    // one memory latency in all; the arithmetic is the general path's, in the same order
+    const float* part = s.part_o + ((int64_t)base * H + h) * L;
+    float li[4];
+    float4 v[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      li[i] = i < np ? lse_p[(int64_t)i * H] : -CUDART_INF_F;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        v[i][k] = i < np ? *reinterpret_cast<const float4*>(part + i * pstride + lane * 4 + k * 128)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m = -CUDART_INF_F;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i < np) m = fmaxf(m, li[i]);
+    float wi[4], tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      wi[i] = li[i] == -CUDART_INF_F ? 0.f : __expf(li[i] - m);
+      if (i < np) tot += wi[i];
+    }
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k].x = fmaf(wi[i], v[i][k].x, acc[k].x);
+        acc[k].y = fmaf(wi[i], v[i][k].y, acc[k].y);
+        acc[k].z = fmaf(wi[i], v[i][k].z, acc[k].z);
+        acc[k].w = fmaf(wi[i], v[i][k].w, acc[k].w);
+      }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      store4<T>(o + lane * 4 + k * 128, make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv));
+    if (lane == 0 && lse_out) lse_out[(int64_t)b * H + h] = tot > 0.f ? m + logf(tot) : -CUDART_INF_F;
+    return;
+  }
   float m = -CUDART_INF_F;
   for (int i = 0; i < np; ++i) m = fmaxf(m, lse_p[(int64_t)i * H]);
   float tot = 0.f;
@@ -424,8 +469,6 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
   const float* part = s.part_o + ((int64_t)base * H + h) * L;
-  const bool vec = (L % 4 == 0) && ((o_s0 | o_s1) % 4 == 0) &&
-                   (reinterpret_cast<uintptr_t>(o_lat) % (4 * sizeof(T)) == 0);
   if (vec && L == 512) {
     // each lane owns four 16-byte chunks of the row; every load of a group of up to four
     // pieces is issued before any of them is used, so the warp waits one memory latency
