@@ -218,3 +218,28 @@ def test_decode_v3_more_units_than_tiles(mla):
     check_close(to_f64(o1), want, "bf16", "v3 decode, 1100 units")
     check_lse(lse1, want_lse, "bf16")
     check_close(to_f64(o0), want, "bf16", "v3 decode, default units")
+
+
+@pytest.mark.parametrize("page", [8, 16, 32, 128])
+def test_decode_v3_tensor_core_page_sizes(mla, page):
+    # The tensor-core path takes pages of 8, 16 and 32 rows (several TMA boxes per 64-key tile,
+    # one per page) and pages of 128 rows (tiles starting inside a page), besides 64: ragged
+    # lengths across page and tile boundaries, a random block table, two split counts.
+    H, E, L, R = mi.V3.n_head, mi.V3.entry, mi.V3.kv_rank, mi.V3.d_rope
+    lens = [1, 37, 200, 64, 129, 8, 450]
+    need = [(n + page - 1) // page for n in lens]
+    nb = sum(need) + 3
+    perm = mi.permutation(180 + page, nb)
+    table = np.full((len(lens), max(need) + 1), -5, np.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    cache = mi.encode(mi.draw("normal", 181, nb * page * E, 0.5), "bf16").reshape(nb, page, E)
+    q = mi.encode(mi.draw("normal", 182, len(lens) * H * E, 0.5), "bf16").reshape(len(lens), H, E)
+    scale = 1.0 / math.sqrt(192)
+    want, want_lse = oracle_decode(q, cache, table, lens, "bf16", L, R, scale)
+    for splits in (0, 3):
+        o, lse = run_decode(mla, q, cache, table, lens, "bf16", L, R, scale, splits)
+        check_close(to_f64(o), want, "bf16", f"page {page}, splits {splits}")
+        check_lse(lse, want_lse, "bf16")

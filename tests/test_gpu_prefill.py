@@ -103,3 +103,25 @@ def test_prefill_tensor_core_rows_without_keys(mla, H, R):
     assert np.array_equal(np.isfinite(lse), fin)
     assert np.max(np.abs(lse[fin] - want_lse[fin])) < 1.2e-2   # ln(1 + 3 * 2^-8): see the decode tests
     assert np.all(got[~fin.all(axis=1)] == 0)
+
+
+@pytest.mark.parametrize("page", [16, 128])
+@pytest.mark.parametrize("H,R", [(128, 64), (64, 0)])
+def test_prefill_tensor_core_page_sizes(mla, page, H, R):
+    # Pages of 16 rows (four TMA boxes per 64-key tile) and of 128 rows (tiles starting inside
+    # a page) on the tensor-core prefill, with pure-prefill and suffix-of-cache sequences.
+    L = 512
+    E = L + R
+    q_lens = [70, 33, 1, 129]
+    kv_lens = [70, 130, 17, 300]
+    table, nb = _tables(kv_lens, page, 190 + page)
+    cache = mi.encode(mi.draw("normal", 191, nb * page * E, 0.5), "bf16").reshape(nb, page, E)
+    T = sum(q_lens)
+    q = mi.encode(mi.draw("normal", 192, T * H * E, 0.5), "bf16").reshape(T, H, E)
+    scale = 1.0 / math.sqrt(192)
+    o, lse, cu = run_prefill(mla, q, cache, table, q_lens, kv_lens, "bf16", L, R, scale)
+    storage = mi.decode_f64(cache.reshape(-1), "bf16")
+    want, want_lse = orc.prefill(mi.decode_f64(q, "bf16"), cu, np.array(kv_lens), storage, 0, page,
+                                 (page * E, E, 1), L, R, table, scale)
+    check_close(to_f64(o), want, "bf16", f"prefill page {page} H={H} R={R}")
+    assert np.max(np.abs(lse - want_lse)) < 1.2e-2   # ln(1 + 3 * 2^-8): see the decode tests
