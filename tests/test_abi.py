@@ -115,3 +115,17 @@ def test_bounded_wait_check_rejects_bad_limits_without_a_launch(mla):
         with pytest.raises(mla.MlaError) as e:
             mla.mla_check_bounded_wait(limit, stream=0)
         assert e.value.status == mla.MLA_ERR_INVALID_ARG
+
+
+def test_concat_in_place_without_rope_moves_nothing(mla):
+    # nope is q_cat_out's own first L columns (same data pointer and strides) and R = 0: the
+    # latent columns are already in place, so the call returns without a launch
+    lib = mla.lib()
+    T, H, L = 4, 8, 16
+    out = _contig([T, H, L])
+    nope = _view([T, H, L], [H * L, L, 1], 0x10000)
+    rope = _contig([T, H, 0])
+    assert lib.mla_concat_q(1, out, nope, rope, None) == mla.MLA_OK
+    # the same with the q_cat_out of a rope-carrying layout still validates its widths first
+    assert lib.mla_concat_q(1, _contig([T, H, L + 4]), _view([T, H, L], [H * (L + 4), L + 4, 1], 0x10000),
+                            _contig([T, H, 3]), None) == mla.MLA_ERR_INVALID_ARG
