@@ -333,6 +333,28 @@ def test_prefill_query_zero_and_prefill_decode_consistency():
         assert np.array_equal(o[r], od[0]) and np.array_equal(lse[r], ld[0])
 
 
+def test_prefill_rows_before_the_first_cached_row_see_nothing():
+    # More queries than cached rows: queries at positions below 0 attend no row (o = 0,
+    # lse = -inf, as for an empty sequence); the others equal decode over their prefix.
+    H, L, R, page = 2, 8, 2, 4
+    kv_lens, q_lens = [3, 0], [5, 2]
+    storage, table, E = _paged_case(H, L, R, page, [3, 1], 62)
+    T = sum(q_lens)
+    q = mi.decode_f64(mi.normal(63, T * H * E), "f32").reshape(T, H, E)
+    cu = np.array([0, 5, 7])
+    o, lse = orc.prefill(q, cu, np.array(kv_lens), storage, 0, page, (page * E, E, 1), L, R, table, 0.5)
+    for r in range(T):
+        b = 0 if r < 5 else 1
+        pos = kv_lens[b] - q_lens[b] + (r - cu[b])
+        if pos < 0:
+            assert np.all(o[r] == 0) and np.all(lse[r] == -np.inf)
+        else:
+            od, ld = orc.decode(q[r][None], storage, 0, page, (page * E, E, 1), L, R,
+                                table[b:b + 1], np.array([pos + 1]), 0.5)
+            assert np.array_equal(o[r], od[0]) and np.array_equal(lse[r], ld[0])
+    assert sum(kv_lens[b] - q_lens[b] + i < 0 for b in range(2) for i in range(q_lens[b])) == 4
+
+
 def test_stepwise_decode_through_appended_cache():
     # Rows are appended one step at a time; each step equals a full recompute (memra gate 2).
     H, P, R, V, L = 4, 24, 8, 32, 64
