@@ -167,6 +167,20 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     ut[w] = t;
   }
   __syncthreads();
+  // the first sequence of each unit's range: the b with pre[b] <= unit_tile[w] < pre[b + 1]
+  for (int w = threadIdx.x; w < W; w += blockDim.x) {
+    const int t0 = ut[w];
+    int bw = B;
+    if (t0 < total && t0 < ut[w + 1]) {
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= t0) lo = mid; else hi = mid - 1;
+      }
+      bw = lo;
+    }
+    s.unit_seq[w] = bw;
+  }
   if (threadIdx.x == 0) carry_sh = 0;
   __syncthreads();
   // pass 2: units touching each sequence, and partial-slot bases
@@ -189,7 +203,12 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     int tot;
     const int ex = block_exclusive_scan(np > 1 ? np : 0, warp_tot, &tot);
     const int carry = carry_sh;
-    if (b < B) s.piece_base[b] = carry + ex;
+    if (b < B) {
+      s.piece_base[b] = carry + ex;
+      // everything a tensor-core walker needs about b in one 16-byte load
+      const int len = min(max(seq_lens[b], 0), cap);
+      s.seqinfo[b] = make_int4(pre[b], len, np, carry + ex - fu);
+    }
     __syncthreads();
     if (threadIdx.x == 0) carry_sh = carry + tot;
     __syncthreads();

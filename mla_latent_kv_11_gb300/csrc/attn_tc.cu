@@ -78,6 +78,7 @@ __device__ unsigned g_tc_err = 0;
 
 constexpr int kRows = 128;                // M: query rows per tile
 constexpr int kKeysT = 64;                // keys per tile
+static_assert(kKeysT == kTile, "a decode key tile is a schedule tile");
 constexpr int kBoxBytesK = kKeysT * 128;  // one 64-column box of a key tile (8 KB)
 constexpr int kRopeHalf = 32;             // rope columns per CTA
 constexpr int kRopeBoxBytes = kKeysT * kRopeHalf * 2;   // 4 KB
@@ -215,12 +216,7 @@ struct Walker {
         active = false;
         return;
       }
-      int lo = 0, hi = p.B;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.sched.tile_prefix[mid] <= t) lo = mid; else hi = mid - 1;
-      }
-      b = lo;
+      b = p.sched.unit_seq[unit];   // the schedule's first sequence of this unit
     } else {
       const int total = p.item_prefix[p.B];
       g = total - 1 - unit;
@@ -231,17 +227,17 @@ struct Walker {
     if (!active) return false;
     if (p.mode == 0) {
       if (t >= t1) return false;
-      while (p.sched.tile_prefix[b + 1] <= t) ++b;
-      const int pre = p.sched.tile_prefix[b];
-      const int seg_end = min(t1, p.sched.tile_prefix[b + 1]);
-      const int len = min(max(p.seq_lens[b], 0), p.cap);
+      // {first tile, clamped length, pieces, slot base - first unit}: one 16-byte load a segment
+      int4 si = p.sched.seqinfo[b];
+      while (si.x + (si.y + kKeysT - 1) / kKeysT <= t) si = p.sched.seqinfo[++b];
+      const int seg_end = min(t1, si.x + (si.y + kKeysT - 1) / kKeysT);
       s.b = b;
       s.tok0 = b;
       s.ntok = 1;
-      s.k0 = (t - pre) * kKeysT;
-      s.k1 = min((seg_end - pre) * kKeysT, len);
+      s.k0 = (t - si.x) * kKeysT;
+      s.k1 = min((seg_end - si.x) * kKeysT, si.y);
       s.pos0 = 0x3fffffff;
-      s.slot = p.sched.npieces[b] == 1 ? -1 : p.sched.piece_base[b] + (unit - p.sched.first_unit[b]);
+      s.slot = si.z == 1 ? -1 : si.w + unit;
       t = seg_end;
       return true;
     }
@@ -634,21 +630,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (nt > 0) {
         const __nv_bfloat16* qrow = p.q + (int64_t)(sg.tok0 + t_in_tile) * p.q_s0 + (int64_t)head * p.q_s1;
-        for (int c = 0; c < 4 + (kRope ? 1 : 0); ++c) {
-          // latent chunk c: 64 values; chunk 4: this CTA's 32 rope values (upper columns zero)
-          const __nv_bfloat16* src = c < 4 ? qrow + col0 + c * 64 : qrow + rope0;
-          const int chunks = c < 4 ? 8 : 4;
+        for (int c = 0; c < 4; ++c) {
+          // latent chunk c: 64 values, 32 columns
+          const __nv_bfloat16* src = qrow + col0 + c * 64;
           uint32_t v[32];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_valid && i < chunks) w = *reinterpret_cast<const uint4*>(src + i * 8);
+            if (row_valid) w = *reinterpret_cast<const uint4*>(src + i * 8);
             v[4 * i] = w.x;
             v[4 * i + 1] = w.y;
             v[4 * i + 2] = w.z;
             v[4 * i + 3] = w.w;
           }
           tmem_st32u(tmem + lane_addr + kTmemQ + c * 32, v);
+        }
+        if (kRope) {
+          // this CTA's 32 rope values: exactly 16 columns. The row-sum columns l follow them, and
+          // the softmax group may still be about to read the current segment's l, so nothing
+          // beyond the rope's 16 columns may be written here.
+          uint32_t v[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row_valid) w = *reinterpret_cast<const uint4*>(qrow + rope0 + i * 8);
+            v[4 * i] = w.x;
+            v[4 * i + 1] = w.y;
+            v[4 * i + 2] = w.z;
+            v[4 * i + 3] = w.w;
+          }
+          tmem_st16u(tmem + lane_addr + kTmemQ + 128, v);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -958,34 +969,6 @@ __global__ void prefill_items_kernel(const int32_t* __restrict__ cu_q, int B, in
   }
 }
 
-// ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
-                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {s1_bytes, s2_bytes};
-  cuuint32_t box[3] = {b0, b1, b2};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int kRope>
 int max_clusters() {
   static std::mutex mu;
@@ -1028,6 +1011,40 @@ cudaError_t launch_tc(const TcParams& p, const CUtensorMap& km, const CUtensorMa
 }
 
 }  // namespace
+
+// ------------------------------------------------------------------ host side
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool tensor_maps_available() { return encode_fn() != nullptr; }
+
+bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 
 bool tc_attention_supported(mla_dtype dt, int H, int L, int R, bool decode, const CacheView& cv,
                             const View3& q, const View3& o) {

@@ -1,10 +1,9 @@
 // Step 2 (q concat) and step 3 (paged latent cache write): pure bit copies.
 //
 // Both move whole rows. When every row start and row length is a multiple of
-// 16 bytes the copy goes in 16-byte vectors (uint4), one vector per thread,
-// consecutive threads on consecutive vectors of a row, so a warp moves 512
-// contiguous bytes; otherwise it falls back to element copies of the same
-// order. The element type never matters: bits are moved as integers, so NaN
+// 16 bytes the copy goes in 16-byte vectors (uint4), consecutive lanes on
+// consecutive vectors of a row; otherwise it falls back to element copies of
+// the same order. The element type never matters: bits are moved as integers, so NaN
 // payloads and signed zeros survive unchanged.
 #include <cstdint>
 
@@ -20,27 +19,45 @@ template <> struct Word<16> { using T = uint4; };
 template <> struct Word<4> { using T = uint32_t; };
 template <> struct Word<2> { using T = uint16_t; };
 
+// Rows are spread over groups of G lanes (G a power of two, 8..32, at least the row's word
+// count when that is below 32): a group handles one row, its lanes stride over the row's
+// words, so a row's index arithmetic (a 32-bit divide, a slot lookup) is done once per row,
+// not once per word, and short rows (the 8 words of the rope columns alone) still fill the
+// warp.
+struct RowSplit {
+  int G;        // lanes per row group
+  int shift;    // log2(G)
+};
+
+__device__ __forceinline__ void row_lane(const RowSplit rs, int64_t& first_row, int64_t& row_step, int& c0) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int per_warp = 32 >> rs.shift;
+  first_row = gwarp * per_warp + (lane >> rs.shift);
+  row_step = nwarps * per_warp;
+  c0 = lane & (rs.G - 1);
+}
+
 // q_cat[t,h,0:L] = nope[t,h,:]; q_cat[t,h,L:L+R] = rope[t,h,:] (rope s1 may be 0).
 // Counts and strides are in units of W (the copy word); L and R are multiples
-// of the word on the vector path.
+// of the word on the vector path. rows = T * H < 2^31.
 template <typename W>
 __global__ void __launch_bounds__(256) concat_q_kernel(
     W* __restrict__ out, int64_t o_s0, int64_t o_s1, const W* __restrict__ nope, int64_t n_s0,
-    int64_t n_s1, const W* __restrict__ rope, int64_t r_s0, int64_t r_s1, int64_t H, int64_t Lw,
-    int64_t Rw, int64_t total) {
+    int64_t n_s1, const W* __restrict__ rope, int64_t r_s0, int64_t r_s1, int32_t H, int32_t Lw,
+    int32_t Rw, int32_t rows, RowSplit rs) {
   pdl_enter();
-  const int64_t Ew = Lw + Rw;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = i / Ew;
-    const int64_t c = i - row * Ew;
-    const int64_t t = row / H, h = row - t * H;
-    W v;
-    if (c < Lw)
-      v = nope[t * n_s0 + h * n_s1 + c];
-    else
-      v = rope[t * r_s0 + h * r_s1 + (c - Lw)];
-    out[t * o_s0 + h * o_s1 + c] = v;
+  const int Ew = Lw + Rw;
+  int64_t r, step;
+  int c0;
+  row_lane(rs, r, step, c0);
+  for (; r < rows; r += step) {
+    const int t = (int)r / H, h = (int)r - t * H;
+    W* o = out + t * o_s0 + h * o_s1;
+    const W* nr = nope + t * n_s0 + h * n_s1;
+    const W* rr = rope + t * r_s0 + h * r_s1 - Lw;
+    for (int c = c0; c < Ew; c += rs.G) o[c] = c < Lw ? nr[c] : rr[c];
   }
 }
 
@@ -49,29 +66,43 @@ template <typename W>
 __global__ void __launch_bounds__(256) cache_write_kernel(
     W* __restrict__ cache, int64_t c_blk, int64_t c_row, int64_t num_rows, int32_t page,
     const W* __restrict__ kv_c, int64_t k_s0, const W* __restrict__ k_pe, int64_t p_s0,
-    const int64_t* __restrict__ slots, int64_t Lw, int64_t Rw, int64_t total) {
+    const int64_t* __restrict__ slots, int32_t Lw, int32_t Rw, int64_t T, RowSplit rs) {
   pdl_enter();
-  const int64_t Ew = Lw + Rw;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t tok = i / Ew;
-    const int64_t c = i - tok * Ew;
+  const int Ew = Lw + Rw;
+  int64_t tok, step;
+  int c0;
+  row_lane(rs, tok, step, c0);
+  for (; tok < T; tok += step) {
     const int64_t s = slots[tok];
     if (s < 0) continue;  // padding
     if (s >= num_rows) {  // would land outside the view: skip and record
-      if (c == 0) atomicOr(&g_copy_err, kErrDeviceData);
+      if (c0 == 0) atomicOr(&g_copy_err, kErrDeviceData);
       continue;
     }
     const int64_t blk = s / page, r = s - blk * page;
-    const W v = c < Lw ? kv_c[tok * k_s0 + c] : k_pe[tok * p_s0 + (c - Lw)];
-    cache[blk * c_blk + r * c_row + c] = v;
+    W* o = cache + blk * c_blk + r * c_row;
+    const W* kr = kv_c + tok * k_s0;
+    const W* pr = k_pe + tok * p_s0 - Lw;
+    for (int c = c0; c < Ew; c += rs.G) o[c] = c < Lw ? kr[c] : pr[c];
   }
+}
+
+RowSplit row_split(int64_t words) {
+  RowSplit rs{32, 5};
+  while (rs.G > 8 && rs.G / 2 >= words) {
+    rs.G /= 2;
+    rs.shift -= 1;
+  }
+  return rs;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-int grid_for(int64_t total) {
-  const int64_t want = (total + 255) / 256;
+// Enough 256-thread blocks for one row group per row, capped at 16 blocks per SM (the
+// kernels stride over the rest).
+int grid_for(int64_t rows, const RowSplit& rs) {
+  const int64_t rows_per_block = 256 / rs.G;
+  const int64_t want = (rows + rows_per_block - 1) / rows_per_block;
   const int64_t cap = (int64_t)device_sm_count() * 16;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
@@ -82,6 +113,8 @@ cudaError_t launch_concat_q(mla_dtype dt, const View3& out, const View3& nope, c
                             cudaStream_t st) {
   const int64_t es = dt == MLA_F32 ? 4 : 2;
   const int64_t T = out.n0, H = out.n1, L = nope.n2, R = rope.n2;
+  const int64_t rows = T * H;
+  if (rows >= INT32_MAX || L + R >= INT32_MAX / 4) return cudaErrorInvalidValue;
   const int64_t per = 16 / es;  // elements per 16-byte word
   bool vec = aligned16(out.data) && aligned16(nope.data) && (R == 0 || aligned16(rope.data)) &&
              L % per == 0 && R % per == 0 && out.s0 % per == 0 && out.s1 % per == 0 &&
@@ -89,22 +122,20 @@ cudaError_t launch_concat_q(mla_dtype dt, const View3& out, const View3& nope, c
              (R == 0 || (rope.s0 % per == 0 && rope.s1 % per == 0));
   const void* rp = R == 0 ? nope.data : rope.data;  // never read when R == 0
   if (vec) {
-    const int64_t total = T * H * (L + R) / per;
-    return launch_k(concat_q_kernel<uint4>, grid_for(total), 256, 0, st,
+    const RowSplit rs = row_split((L + R) / per);
+    return launch_k(concat_q_kernel<uint4>, grid_for(rows, rs), 256, 0, st,
         (uint4*)out.data, out.s0 / per, out.s1 / per, (const uint4*)nope.data, nope.s0 / per,
-        nope.s1 / per, (const uint4*)rp, rope.s0 / per, rope.s1 / per, H, L / per, R / per, total);
-  } else {
-    const int64_t total = T * H * (L + R);
-    if (es == 4)
-      return launch_k(concat_q_kernel<uint32_t>, grid_for(total), 256, 0, st,
-          (uint32_t*)out.data, out.s0, out.s1, (const uint32_t*)nope.data, nope.s0, nope.s1,
-          (const uint32_t*)rp, rope.s0, rope.s1, H, L, R, total);
-    else
-      return launch_k(concat_q_kernel<uint16_t>, grid_for(total), 256, 0, st,
-          (uint16_t*)out.data, out.s0, out.s1, (const uint16_t*)nope.data, nope.s0, nope.s1,
-          (const uint16_t*)rp, rope.s0, rope.s1, H, L, R, total);
+        nope.s1 / per, (const uint4*)rp, rope.s0 / per, rope.s1 / per, (int32_t)H, (int32_t)(L / per),
+        (int32_t)(R / per), (int32_t)rows, rs);
   }
-  return cudaGetLastError();
+  const RowSplit rs = row_split(L + R);
+  if (es == 4)
+    return launch_k(concat_q_kernel<uint32_t>, grid_for(rows, rs), 256, 0, st,
+        (uint32_t*)out.data, out.s0, out.s1, (const uint32_t*)nope.data, nope.s0, nope.s1,
+        (const uint32_t*)rp, rope.s0, rope.s1, (int32_t)H, (int32_t)L, (int32_t)R, (int32_t)rows, rs);
+  return launch_k(concat_q_kernel<uint16_t>, grid_for(rows, rs), 256, 0, st,
+      (uint16_t*)out.data, out.s0, out.s1, (const uint16_t*)nope.data, nope.s0, nope.s1,
+      (const uint16_t*)rp, rope.s0, rope.s1, (int32_t)H, (int32_t)L, (int32_t)R, (int32_t)rows, rs);
 }
 
 cudaError_t launch_cache_write(mla_dtype dt, const View3& cache, const View3& kv_c,
@@ -114,27 +145,25 @@ cudaError_t launch_cache_write(mla_dtype dt, const View3& cache, const View3& kv
   const int64_t per = 16 / es;
   const int64_t rows = cache.n0 * cache.n1;
   const int32_t page = (int32_t)cache.n1;
+  if (L + R >= INT32_MAX / 4) return cudaErrorInvalidValue;
   bool vec = aligned16(cache.data) && aligned16(kv_c.data) && (R == 0 || aligned16(k_pe.data)) &&
              L % per == 0 && R % per == 0 && cache.s0 % per == 0 && cache.s1 % per == 0 &&
              kv_c.s0 % per == 0 && (R == 0 || k_pe.s0 % per == 0);
   const void* kp = R == 0 ? kv_c.data : k_pe.data;
   if (vec) {
-    const int64_t total = T * (L + R) / per;
-    return launch_k(cache_write_kernel<uint4>, grid_for(total), 256, 0, st,
+    const RowSplit rs = row_split((L + R) / per);
+    return launch_k(cache_write_kernel<uint4>, grid_for(T, rs), 256, 0, st,
         (uint4*)cache.data, cache.s0 / per, cache.s1 / per, rows, page, (const uint4*)kv_c.data,
-        kv_c.s0 / per, (const uint4*)kp, k_pe.s0 / per, slots, L / per, R / per, total);
-  } else {
-    const int64_t total = T * (L + R);
-    if (es == 4)
-      return launch_k(cache_write_kernel<uint32_t>, grid_for(total), 256, 0, st,
-          (uint32_t*)cache.data, cache.s0, cache.s1, rows, page, (const uint32_t*)kv_c.data,
-          kv_c.s0, (const uint32_t*)kp, k_pe.s0, slots, L, R, total);
-    else
-      return launch_k(cache_write_kernel<uint16_t>, grid_for(total), 256, 0, st,
-          (uint16_t*)cache.data, cache.s0, cache.s1, rows, page, (const uint16_t*)kv_c.data,
-          kv_c.s0, (const uint16_t*)kp, k_pe.s0, slots, L, R, total);
+        kv_c.s0 / per, (const uint4*)kp, k_pe.s0 / per, slots, (int32_t)(L / per), (int32_t)(R / per), T, rs);
   }
-  return cudaGetLastError();
+  const RowSplit rs = row_split(L + R);
+  if (es == 4)
+    return launch_k(cache_write_kernel<uint32_t>, grid_for(T, rs), 256, 0, st,
+        (uint32_t*)cache.data, cache.s0, cache.s1, rows, page, (const uint32_t*)kv_c.data,
+        kv_c.s0, (const uint32_t*)kp, k_pe.s0, slots, (int32_t)L, (int32_t)R, T, rs);
+  return launch_k(cache_write_kernel<uint16_t>, grid_for(T, rs), 256, 0, st,
+      (uint16_t*)cache.data, cache.s0, cache.s1, rows, page, (const uint16_t*)kv_c.data,
+      kv_c.s0, (const uint16_t*)kp, k_pe.s0, slots, (int32_t)L, (int32_t)R, T, rs);
 }
 
 unsigned copy_errors_read_clear() {

@@ -117,6 +117,8 @@ DecodeWsLayout decode_ws_layout(int64_t B, int64_t H, int64_t L, int64_t units) 
   l.off_np = off;     off = up(off + sizeof(int32_t) * B);
   l.off_base = off;   off = up(off + sizeof(int32_t) * B);
   l.off_unit = off;   off = up(off + sizeof(int32_t) * (units + 1));
+  l.off_useq = off;   off = up(off + sizeof(int32_t) * units);
+  l.off_seqinfo = off; off = up(off + sizeof(int4) * B);
   const int64_t pieces = B + units;
   l.off_part_o = off;   off = up(off + sizeof(float) * pieces * H * L);
   l.off_part_lse = off; off = up(off + sizeof(float) * pieces * H);
@@ -132,6 +134,8 @@ DecodeSched decode_sched_from_ws(void* ws, const DecodeWsLayout& lay, int32_t B,
   s.npieces = reinterpret_cast<int32_t*>(p + lay.off_np);
   s.piece_base = reinterpret_cast<int32_t*>(p + lay.off_base);
   s.unit_tile = reinterpret_cast<int32_t*>(p + lay.off_unit);
+  s.unit_seq = reinterpret_cast<int32_t*>(p + lay.off_useq);
+  s.seqinfo = reinterpret_cast<int4*>(p + lay.off_seqinfo);
   s.part_o = reinterpret_cast<float*>(p + lay.off_part_o);
   s.part_lse = reinterpret_cast<float*>(p + lay.off_part_lse);
   s.units = units;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -72,6 +73,8 @@ struct DecodeSched {
   int32_t* npieces;      // [B]   work units touching b (0 for an empty sequence)
   int32_t* piece_base;   // [B]   first partial slot of b (if npieces[b] > 1)
   int32_t* unit_tile;    // [units+1] first global tile of each work unit (the last entry: total)
+  int32_t* unit_seq;     // [units]   first sequence of each unit's range (B for an empty unit)
+  int4* seqinfo;         // [B] {tile_prefix[b], clamped length, npieces[b], piece_base[b] - first_unit[b]}
   float* part_o;         // [max_pieces, H, L] normalised partial outputs
   float* part_lse;       // [max_pieces, H]    their natural-log LSE
   int32_t units;         // number of work units W
@@ -80,13 +83,20 @@ struct DecodeSched {
 
 // Workspace layout of mla_decode for (B, H, L, units).
 struct DecodeWsLayout {
-  size_t off_prefix, off_first, off_np, off_base, off_unit, off_part_o, off_part_lse, total;
+  size_t off_prefix, off_first, off_np, off_base, off_unit, off_useq, off_seqinfo, off_part_o, off_part_lse,
+      total;
 };
 DecodeWsLayout decode_ws_layout(int64_t B, int64_t H, int64_t L, int64_t units);
 DecodeSched decode_sched_from_ws(void* ws, const DecodeWsLayout& lay, int32_t B, int32_t units);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// A 3-D bf16 TMA map (dims innermost first, strides of dims 1 and 2 in bytes, box b0 x b1 x b2).
+bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz);
+// True once the driver's tensor-map encoder has been found.
+bool tensor_maps_available();
 
 // ---- launchers (return cudaSuccess or the launch error) -------------------
 cudaError_t launch_concat_q(mla_dtype dt, const View3& out, const View3& nope, const View3& rope,

@@ -156,6 +156,43 @@ def test_decode_v3_consecutive_empty_sequences(mla, splits):
             assert np.all(got[b] == 0) and np.all(lse[b] == -np.inf)
 
 
+def test_decode_v3_segment_boundaries_repeated(mla):
+    # A work unit that finishes one sequence and goes on to the next hands the tensor memory
+    # from one segment to the next while the previous segment's epilogue may still read its row
+    # sums; whether that goes wrong depends on timing, so the same split batch is decoded many
+    # times (fresh, differently filled workspaces) and every result is checked.
+    import torch
+    H, E, L, R = mi.V3.n_head, mi.V3.entry, mi.V3.kv_rank, mi.V3.d_rope
+    lens = [0, 0, 70, 0, 0, 0, 129, 0, 64, 0, 0, 1, 0]
+    page = 64
+    need = [(n + page - 1) // page for n in lens]
+    nb = sum(need) + 2
+    perm = mi.permutation(81, nb)
+    table = np.full((len(lens), max(need) + 1), -3, np.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    cache_bits = mi.encode(mi.draw("normal", 82, nb * page * E, 0.5), "bf16").reshape(nb, page, E)
+    q_bits = mi.encode(mi.draw("normal", 83, len(lens) * H * E, 0.5), "bf16").reshape(len(lens), H, E)
+    scale = 1.0 / math.sqrt(192)
+    want, want_lse = oracle_decode(q_bits, cache_bits, table, lens, "bf16", L, R, scale)
+    B = len(lens)
+    q, cache = to_dev(q_bits, "bf16"), to_dev(cache_bits, "bf16")
+    table_d = torch.from_numpy(table).cuda()
+    lens_d = torch.from_numpy(np.asarray(lens, np.int32)).cuda()
+    for rep in range(24):
+        splits = (2, 3, 5)[rep % 3]
+        ws = torch.full((mla.mla_decode_workspace_size(B, H, L, splits),), (0x00, 0x41, 0xFF)[rep % 3],
+                        dtype=torch.uint8, device="cuda")
+        o = poisoned((B, H, L), "bf16")
+        lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
+        mla.mla_decode(o, q, cache, table_d, lens_d, L, R, scale, lse_out=lse, num_splits=splits, workspace=ws)
+        mla.mla_device_error()
+        check_close(to_f64(o), want, "bf16", f"repeat {rep}, splits {splits}")
+        check_lse(lse.cpu().numpy().astype(np.float64), want_lse, "bf16")
+
+
 def test_decode_large_variable_lengths_sampled(mla):
     # B=64 sequences of 1K..16K rows, auto split count (the bench configuration), sampled check.
     w = mi.v3_decode_large(materialize_cache=True)
