@@ -202,7 +202,8 @@ mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tenso
  *   until the process exits; a batch whose scratch would not fit (about
  *   (B + work units) * H * L * 4 bytes) returns MLA_ERR_UNSUPPORTED. The call
  *   allocates nothing. Its first call on a device looks up the array's device
- *   address (once per device); make that first call before any stream capture.
+ *   address (once per device and context: again after a reset of the device);
+ *   make that first call before any stream capture.
  *   All calls share the array: calls whose kernels overlap on the GPU race and
  *   must be serialised by the caller. */
 mla_status mla_decode_noalloc(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out,

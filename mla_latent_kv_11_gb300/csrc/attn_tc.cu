@@ -1048,7 +1048,6 @@ bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint
 
 bool tc_attention_supported(mla_dtype dt, int H, int L, int R, bool decode, const CacheView& cv,
                             const View3& q, const View3& o) {
-  if (getenv("MLA_DISABLE_TC") != nullptr) return false;
   if (dt != MLA_BF16 || L != 512 || (R != 0 && R != 64)) return false;
   if (decode ? H != 128 : (H != 128 && H != 64)) return false;
   const int page = cv.page;

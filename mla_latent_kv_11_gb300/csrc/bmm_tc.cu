@@ -215,7 +215,6 @@ cudaError_t launch(const CUtensorMap& am, const CUtensorMap& bm, const CUtensorM
 }  // namespace
 
 bool bmm_tc_supported(mla_dtype dt, const View3& out, const View3& a, const View3& b) {
-  if (getenv("MLA_DISABLE_TC") != nullptr) return false;
   if (dt != MLA_BF16 || !encode()) return false;
   const int64_t K = a.n2, N = b.n2;
   if (K % 64 != 0 || N % 128 != 0 || a.n1 < 1) return false;

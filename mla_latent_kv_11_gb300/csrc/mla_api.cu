@@ -32,8 +32,6 @@ int64_t numel(const mla_tensor& t) {
   return n;
 }
 
-size_t esize(mla_dtype dt) { return dt == MLA_F32 ? 4 : 2; }
-
 // Well-formedness of one view: rank, non-negative sizes, non-null data when
 // non-empty, innermost stride 1 (the one layout rule the source tests assert).
 mla_status check_view(const mla_tensor& t, int rank, const char* name) {
@@ -164,10 +162,70 @@ static cudaError_t launch_bmm(mla_dtype dt, const View3& out, const View3& a, co
   return launch_bmm_simt(dt, out, a, b, st);
 }
 
-// Work units of the split-KV decode: explicit, or two per SM.
-static int32_t decode_units(int32_t num_splits) {
+// Work units of the general split-KV decode: explicit, or two per SM.
+int32_t decode_units(int32_t num_splits) {
   if (num_splits > 0) return num_splits;
   return 2 * device_sm_count();
+}
+
+mla_status check_decode_args(mla_dtype dtype, const mla_tensor& o_lat_out, const mla_tensor& q_cat,
+                             const mla_tensor& cache, const int32_t* block_table, int64_t block_table_stride,
+                             int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim,
+                             float softmax_scale, int32_t num_splits, DecodeCall* out) {
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat, 3, "q_cat"));
+  MLA_TRY(check_view(o_lat_out, 3, "o_lat_out"));
+  const int64_t B = q_cat.shape[0], H = q_cat.shape[1];
+  const int64_t L = kv_lora_rank, R = rope_dim;
+  if (L <= 0 || R < 0) return fail(MLA_ERR_INVALID_ARG, "kv_lora_rank must be > 0 and rope_dim >= 0");
+  if (q_cat.shape[2] != L + R)
+    return fail(MLA_ERR_INVALID_ARG, "q_cat width %lld != L + R = %lld", (long long)q_cat.shape[2],
+                (long long)(L + R));
+  if (o_lat_out.shape[0] != B || o_lat_out.shape[1] != H || o_lat_out.shape[2] != L)
+    return fail(MLA_ERR_INVALID_ARG, "o_lat_out must be [B,H,L] = [%lld,%lld,%lld]", (long long)B,
+                (long long)H, (long long)L);
+  MLA_TRY(check_cache(cache, L + R, "cache"));
+  if (num_splits < 0) return fail(MLA_ERR_INVALID_ARG, "num_splits < 0");
+  out->B = B;
+  out->H = H;
+  out->L = L;
+  out->R = R;
+  out->empty = B == 0 || H == 0;
+  if (out->empty) return MLA_OK;
+  if (B > INT32_MAX / 2 || H > 4096) return fail(MLA_ERR_UNSUPPORTED, "batch or head count too large");
+  if (block_table == nullptr || seq_lens == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "block_table and seq_lens must be non-null");
+  if (max_blocks <= 0 || block_table_stride < max_blocks)
+    return fail(MLA_ERR_INVALID_ARG, "need 0 < max_blocks <= block_table_stride");
+  if (L > 512) return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank %lld > 512", (long long)L);
+  if (L + R > 1024) return fail(MLA_ERR_UNSUPPORTED, "entry width %lld > 1024", (long long)(L + R));
+  out->cv = CacheView{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
+                      (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
+  out->qv = view3(q_cat);
+  out->ov = view3(o_lat_out);
+  out->tc = softmax_scale > 0.f &&
+            tc_attention_supported(dtype, (int)H, (int)L, (int)R, true, out->cv, out->qv, out->ov);
+  // work units: one per 2-CTA cluster on the tensor-core path, else from num_splits
+  out->units = out->tc ? tc_decode_units(num_splits) : decode_units(num_splits);
+  return MLA_OK;
+}
+
+mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, const int32_t* block_table,
+                      int64_t block_table_stride, int32_t max_blocks, const int32_t* seq_lens, float softmax_scale,
+                      void* scratch, const DecodeWsLayout& lay, cudaStream_t st) {
+  const DecodeSched s = decode_sched_from_ws(scratch, lay, (int32_t)dc.B, dc.units);
+  const int32_t B = (int32_t)dc.B, H = (int32_t)dc.H, L = (int32_t)dc.L, R = (int32_t)dc.R;
+  MLA_TRY(cuda_status(launch_decode_schedule(seq_lens, B, max_blocks, dc.cv.page, s, st), "mla_decode schedule"));
+  if (dc.tc) {
+    MLA_TRY(cuda_status(launch_decode_tc(dc.ov, lse_out, dc.qv, dc.cv, block_table, block_table_stride,
+                                         max_blocks, seq_lens, B, H, L, R, softmax_scale, s, st),
+                        "mla_decode split kernel (tensor cores)"));
+  } else {
+    MLA_TRY(cuda_status(launch_decode_simt(dtype, dc.ov, lse_out, dc.qv, dc.cv, block_table, block_table_stride,
+                                           max_blocks, seq_lens, B, H, L, R, softmax_scale, s, st),
+                        "mla_decode split kernel"));
+  }
+  return cuda_status(launch_decode_combine(dtype, dc.ov, lse_out, seq_lens, B, H, L, s, st), "mla_decode combine");
 }
 
 }  // namespace mla
@@ -278,58 +336,19 @@ mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla
                       int32_t rope_dim, float softmax_scale, int32_t num_splits, void* workspace,
                       size_t workspace_bytes, void* stream) {
   g_msg[0] = 0;
-  MLA_TRY(check_dtype(dtype));
-  MLA_TRY(check_view(q_cat, 3, "q_cat"));
-  MLA_TRY(check_view(o_lat_out, 3, "o_lat_out"));
-  const int64_t B = q_cat.shape[0], H = q_cat.shape[1];
-  const int64_t L = kv_lora_rank, R = rope_dim;
-  if (L <= 0 || R < 0) return fail(MLA_ERR_INVALID_ARG, "kv_lora_rank must be > 0 and rope_dim >= 0");
-  if (q_cat.shape[2] != L + R)
-    return fail(MLA_ERR_INVALID_ARG, "q_cat width %lld != L + R = %lld", (long long)q_cat.shape[2],
-                (long long)(L + R));
-  if (o_lat_out.shape[0] != B || o_lat_out.shape[1] != H || o_lat_out.shape[2] != L)
-    return fail(MLA_ERR_INVALID_ARG, "o_lat_out must be [B,H,L] = [%lld,%lld,%lld]", (long long)B,
-                (long long)H, (long long)L);
-  MLA_TRY(check_cache(cache, L + R, "cache"));
-  if (num_splits < 0) return fail(MLA_ERR_INVALID_ARG, "num_splits < 0");
-  if (B == 0 || H == 0) return MLA_OK;
-  if (B > INT32_MAX / 2 || H > 4096) return fail(MLA_ERR_UNSUPPORTED, "batch or head count too large");
-  if (block_table == nullptr || seq_lens == nullptr)
-    return fail(MLA_ERR_INVALID_ARG, "block_table and seq_lens must be non-null");
-  if (max_blocks <= 0 || block_table_stride < max_blocks)
-    return fail(MLA_ERR_INVALID_ARG, "need 0 < max_blocks <= block_table_stride");
-  if (L > 512) return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank %lld > 512", (long long)L);
-  if (L + R > 1024) return fail(MLA_ERR_UNSUPPORTED, "entry width %lld > 1024", (long long)(L + R));
-  const DecodeWsLayout lay = decode_ws_layout(B, H, L, decode_units(num_splits));
+  DecodeCall dc;
+  MLA_TRY(check_decode_args(dtype, o_lat_out, q_cat, cache, block_table, block_table_stride, max_blocks,
+                            seq_lens, kv_lora_rank, rope_dim, softmax_scale, num_splits, &dc));
+  if (dc.empty) return MLA_OK;
+  // the workspace is sized for the general work-unit count, which covers the tensor-core one
+  const DecodeWsLayout lay = decode_ws_layout(dc.B, dc.H, dc.L, decode_units(num_splits));
   if (workspace == nullptr || workspace_bytes < lay.total)
     return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes,
                 lay.total);
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  const CacheView cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0],
-                     (int32_t)cache.shape[1], (int32_t)cache.shape[2]};
-  const View3 qv = view3(q_cat), ov = view3(o_lat_out);
-  const bool tc = softmax_scale > 0.f && tc_attention_supported(dtype, (int)H, (int)L, (int)R, true, cv, qv, ov);
-  // work units: one per 2-CTA cluster on the tensor-core path, else from num_splits
-  const int32_t units = tc ? tc_decode_units(num_splits) : decode_units(num_splits);
-  const DecodeSched s = decode_sched_from_ws(workspace, lay, (int32_t)B, units);
-  cudaStream_t st = (cudaStream_t)stream;
-  MLA_TRY(cuda_status(launch_decode_schedule(seq_lens, (int32_t)B, max_blocks, cv.page, s, st),
-                      "mla_decode schedule"));
-  if (tc) {
-    MLA_TRY(cuda_status(launch_decode_tc(ov, lse_out, qv, cv, block_table, block_table_stride,
-                                         max_blocks, seq_lens, (int32_t)B, (int32_t)H, (int32_t)L,
-                                         (int32_t)R, softmax_scale, s, st),
-                        "mla_decode split kernel (tensor cores)"));
-  } else {
-    MLA_TRY(cuda_status(launch_decode_simt(dtype, ov, lse_out, qv, cv, block_table,
-                                           block_table_stride, max_blocks, seq_lens, (int32_t)B,
-                                           (int32_t)H, (int32_t)L, (int32_t)R, softmax_scale, s, st),
-                        "mla_decode split kernel"));
-  }
-  return cuda_status(launch_decode_combine(dtype, ov, lse_out, seq_lens, (int32_t)B, (int32_t)H,
-                                           (int32_t)L, s, st),
-                     "mla_decode combine");
+  return run_decode(dtype, dc, lse_out, block_table, block_table_stride, max_blocks, seq_lens, softmax_scale,
+                    workspace, lay, (cudaStream_t)stream);
 }
 
 size_t mla_prefill_workspace_size(int32_t batch) {

@@ -141,6 +141,29 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
                               int32_t L, int32_t R, float scale, int32_t* item_prefix,
                               cudaStream_t st);
 
+// Work units of the general (CUDA-core) split-KV decode: num_splits, or two per SM.
+int32_t decode_units(int32_t num_splits);
+
+// A decode call after validation: the views the kernels take, the path and its work units.
+struct DecodeCall {
+  int64_t B = 0, H = 0, L = 0, R = 0;
+  bool empty = true;   // nothing to do (B or H is 0)
+  CacheView cv{};
+  View3 qv{}, ov{};
+  bool tc = false;     // tensor-core path
+  int32_t units = 0;
+};
+// The argument checks of mla_decode (every decode entry point uses them, so they report the same
+// codes and messages); fills *out on MLA_OK.
+mla_status check_decode_args(mla_dtype dtype, const mla_tensor& o_lat_out, const mla_tensor& q_cat,
+                             const mla_tensor& cache, const int32_t* block_table, int64_t block_table_stride,
+                             int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim,
+                             float softmax_scale, int32_t num_splits, DecodeCall* out);
+// Schedule, split kernel and combine of a validated decode, with its scratch laid out by `lay`.
+mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, const int32_t* block_table,
+                      int64_t block_table_stride, int32_t max_blocks, const int32_t* seq_lens, float softmax_scale,
+                      void* scratch, const DecodeWsLayout& lay, cudaStream_t st);
+
 // Set (or clear, with MLA_OK) the calling thread's mla_last_error() message.
 mla_status report_status(mla_status st, const char* fmt, ...);
 

@@ -193,22 +193,26 @@ def test_decode_v3_segment_boundaries_repeated(mla):
         check_lse(lse.cpu().numpy().astype(np.float64), want_lse, "bf16")
 
 
-def test_decode_large_variable_lengths_sampled(mla):
-    # B=64 sequences of 1K..16K rows, auto split count (the bench configuration), sampled check.
+@pytest.mark.parametrize("sharp", [1.0, 30.0])
+def test_decode_large_variable_lengths_all_sequences(mla, sharp):
+    # The bench configuration: B=64 sequences of 1K..16K rows, auto split count. Every sequence is
+    # checked against the oracle, so the ones the schedule cuts across two or more work units are
+    # covered along with the shortest and the longest; q x 30 makes the softmax far from uniform,
+    # so the per-tile rescaling and the merge of split sequences are exercised, not averaged away.
     w = mi.v3_decode_large(materialize_cache=True)
     g = w.geom
-    q = mi.encode(mi.draw("normal", 3011, w.batch * g.n_head * g.entry, 0.1), "bf16").reshape(
+    q = mi.encode(mi.draw("normal", 3011, w.batch * g.n_head * g.entry, 0.1 * sharp), "bf16").reshape(
         w.batch, g.n_head, g.entry)
     o, lse = run_decode(mla, q, w.full_cache(), w.block_table, w.seq_lens, "bf16", g.kv_rank,
                         g.d_rope, w.scale)
     got = to_f64(o)
     assert np.all(np.isfinite(got))
-    lens = w.seq_lens
-    ids = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 0, 31, w.batch - 1})
-    want, want_lse = oracle_decode(q, w.full_cache(), w.block_table, lens, "bf16", g.kv_rank,
-                                   g.d_rope, w.scale, ids=ids)
-    check_close(got[ids], want, "bf16", "large decode (sampled sequences)")
-    check_lse(lse[ids], want_lse)
+    want, want_lse = oracle_decode(q, w.full_cache(), w.block_table, w.seq_lens, "bf16", g.kv_rank,
+                                   g.d_rope, w.scale)
+    check_close(got, want, "bf16", f"large decode, q x {sharp}, all sequences")
+    for b in (int(np.argmin(w.seq_lens)), int(np.argmax(w.seq_lens))):
+        check_close(got[b], want[b], "bf16", f"large decode, q x {sharp}, sequence {b} alone")
+    check_lse(lse, want_lse, "bf16")
 
 
 def _ragged_batch(B, H, E, max_len, page, seed, dtype):

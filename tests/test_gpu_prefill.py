@@ -59,6 +59,27 @@ def test_prefill_small_geometries(mla, dims, dtype):
     assert np.max(np.abs(lse - want_lse)) < 1e-3
 
 
+def test_prefill_fp32_production_nope_geometry(mla):
+    # The f32 core at the NoPE production geometry (64 heads, rank 512, no rope, 256-d nope and
+    # v heads: scale 1/sqrt(256)) with the (t_q, t_kv) shapes of the memra prefill gate, pure
+    # prefill and a suffix of a populated cache, held to max-abs 1e-4 and to 1e-4 * max(|o|, 1).
+    H, L, R, page = 64, 512, 0, 64
+    E = L + R
+    q_lens = [4, 3, 17]
+    kv_lens = [4, 9, 17]
+    table, nb = _tables(kv_lens, page, 88)
+    cache = mi.encode(mi.draw("uniform", 89, nb * page * E), "f32").reshape(nb, page, E)
+    q = mi.encode(mi.draw("uniform", 90, sum(q_lens) * H * E), "f32").reshape(sum(q_lens), H, E)
+    scale = 1.0 / math.sqrt(256)
+    o, lse, cu = run_prefill(mla, q, cache, table, q_lens, kv_lens, "f32", L, R, scale)
+    storage = mi.decode_f64(cache.reshape(-1), "f32")
+    want, want_lse = orc.prefill(mi.decode_f64(q, "f32"), cu, np.array(kv_lens), storage, 0, page,
+                                 (page * E, E, 1), L, R, table, scale)
+    info = check_close(to_f64(o), want, "f32", "fp32 prefill, production NoPE geometry")
+    assert info["scaled"] <= 1e-4, info
+    assert np.max(np.abs(lse - want_lse)) < 1e-4
+
+
 def test_prefill_nope_full_size_sampled(mla):
     # 4 x 2048 causal, 64 heads, L=512, R=0; q_lat-like queries ~N(0,1)*0.7, latent rows ~N(0,1).
     H, L, R, page = 64, 512, 0, 64
