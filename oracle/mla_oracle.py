@@ -29,7 +29,13 @@ Readings where the pages are silent (each is listed in the design notes):
     and kv_len cached rows sits at position kv_len - q_len + i and sees rows
     0..pos (P2, "queries a suffix of a populated cache");
   * an empty key range gives o = 0 and lse = -inf;
-  * a negative slot in a slot mapping marks padding and writes nothing.
+  * a negative slot in a slot mapping marks padding and writes nothing;
+  * an fp8 cache holds e4m3 codes; writing one divides the stored value by the
+    cache scale in float32 (correctly rounded) and rounds to nearest e4m3, ties
+    to even, saturating finite values at +-448 (P3 passes a scale to the cache
+    write and descale_q / descale_k to the fp8 decode but prints neither the
+    conversion nor the dequantisation); reading one multiplies the code's value
+    by descale_k, and the query by descale_q.
 """
 from __future__ import annotations
 
@@ -128,6 +134,59 @@ def cache_write(storage: np.ndarray, offset: int, num_blocks: Optional[int], pag
         out[base + cols[:L]] = kv_c[i]
         out[base + cols[L:]] = k_pe[i]
     return out
+
+
+# ---------------------------------------------------------------------------
+# fp8 (e4m3) latent cache (P3: the dense fp8 decode tests store the 576-wide
+# rows as float8 e4m3 and pass descale_q / descale_k; concat_and_cache_mla
+# takes the cache dtype and a scale)
+# ---------------------------------------------------------------------------
+
+def e4m3_value(code) -> np.ndarray:
+    """float64 value of e4m3 codes: 1 sign bit, 4 exponent bits with bias 7 and 3
+    mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); there are no infinities
+    and the two codes with every exponent and mantissa bit set are NaN."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    sign = np.where((c & 0x80) != 0, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (c & 0x7 == 7), np.nan, mag)
+    return sign * mag
+
+
+# every non-negative finite e4m3 value, ascending: codes 0x00 .. 0x7E
+_E4M3_POS = e4m3_value(np.arange(0x7F, dtype=np.uint8))
+
+
+def e4m3_code(x) -> np.ndarray:
+    """e4m3 code of float32 values: round to the nearest representable value, ties to
+    the even code (the one with an even mantissa), finite values beyond 448 saturate to
+    the largest finite code of their sign; signed zeros keep their sign; NaN -> 0x7F."""
+    v = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.abs(v)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 0x7E)   # first value >= |x|
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E4M3_POS[hi] - a
+    d_lo = a - _E4M3_POS[lo]
+    take_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(take_lo & (a <= _E4M3_POS[0x7E]), lo, hi)
+    code = np.where(a >= _E4M3_POS[0x7E], 0x7E, code)                  # saturate (and 448 itself)
+    code = code | np.where(np.signbit(v), 0x80, 0)
+    code = np.where(np.isnan(v), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def cache_write_fp8(storage: np.ndarray, offset: int, num_blocks: Optional[int], page: int,
+                    strides: Sequence[int], kv_c: np.ndarray, k_pe: np.ndarray, slots: np.ndarray,
+                    scale: float) -> np.ndarray:
+    """The cache write into an e4m3 cache (flat uint8 ``storage``): row i becomes the
+    codes of float32(x) / float32(scale) for x in [kv_c[i] | k_pe[i]] (the stored
+    input values, float32-exact), written through ``cache_write``'s addressing."""
+    s32 = np.float32(scale)
+    kc = e4m3_code(np.asarray(kv_c, dtype=np.float32) / s32)
+    kp = e4m3_code(np.asarray(k_pe, dtype=np.float32) / s32)
+    return cache_write(storage, offset, num_blocks, page, strides, kc, kp, slots)
 
 
 def paged_rows(storage: np.ndarray, offset: int, page: int, strides: Sequence[int],
@@ -242,6 +301,18 @@ def decode(q_cat: np.ndarray, storage: np.ndarray, offset: int, page: int,
         os_.append(o)
         ls_.append(lse)
     return np.stack(os_), np.stack(ls_)
+
+
+def decode_fp8(q_cat: np.ndarray, storage: np.ndarray, offset: int, page: int,
+               strides: Sequence[int], L: int, R: int, block_table: np.ndarray,
+               seq_lens: np.ndarray, scale: float, descale_q: float, descale_k: float,
+               batch_ids: Optional[Sequence[int]] = None) -> tuple[np.ndarray, np.ndarray]:
+    """Dense decode over an e4m3 cache (P3, ``flash_mla_with_kvcache_fp8`` with
+    descale_q / descale_k): every cache value is its code's value times descale_k,
+    the query is q_cat times descale_q, and then it is ``decode``."""
+    values = e4m3_value(storage) * float(descale_k)
+    return decode(np.asarray(q_cat) * float(descale_q), values, offset, page, strides, L, R,
+                  block_table, seq_lens, scale, batch_ids)
 
 
 def prefill(q_cat: np.ndarray, cu_seqlens_q: np.ndarray, kv_lens: np.ndarray,

@@ -473,3 +473,119 @@ def test_workload_geometry_matches_the_pages():
     w = mi.write_concat_workload()
     assert w.kv_c.shape == (u["ntok"], u["kv_lora_rank"]) and w.k_pe.shape == (u["ntok"], u["pe"])
     assert len(set(w.slots.tolist())) == u["ntok"] and w.slots.max() < u["num_blocks"] * u["page"]
+
+
+# ---------------------------------------------------------------------------- fp8 (e4m3) cache
+
+def test_e4m3_values_are_the_formats():
+    # 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals at exponent 0, no
+    # infinities, NaN only where every exponent and mantissa bit is set
+    v = orc.e4m3_value(np.arange(256, dtype=np.uint8))
+    assert v[0x38] == 1.0 and v[0x40] == 2.0 and v[0x30] == 0.5
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0            # largest finite
+    assert v[0x08] == 2.0 ** -6 and v[0x01] == 2.0 ** -9     # smallest normal, smallest subnormal
+    assert v[0x07] == 7 * 2.0 ** -9                          # largest subnormal
+    assert v[0x00] == 0.0 and np.signbit(v[0x80]) and v[0x80] == 0.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.sum(np.isnan(v)) == 2
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)                          # codes 0..126 are ascending
+
+
+def test_e4m3_round_trip_and_torch_agree():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    v = orc.e4m3_value(codes)
+    fin = ~np.isnan(v)
+    assert np.array_equal(orc.e4m3_code(v[fin].astype(np.float32)), codes[fin])   # exact values
+    x = (mi.draw("normal", 7001, 200000) * 60.0).astype(np.float32)
+    x = x[np.abs(x) < 448]                                    # torch's cast does not saturate
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.e4m3_code(x), t)
+
+
+def test_e4m3_ties_to_even_and_saturation():
+    c = orc.e4m3_code(np.array([1 + 1 / 16, 1 + 3 / 16, 2.0 ** -10, 3 * 2.0 ** -10,
+                                449.0, 464.0, 1e6, -1e6, -0.0, np.nan], np.float32))
+    assert c.tolist() == [0x38, 0x3A, 0x00, 0x02, 0x7E, 0x7E, 0x7E, 0xFE, 0x80, 0x7F]
+
+
+def test_fp8_cache_write_is_the_scaled_code_and_does_not_bleed():
+    T, L, R, page, nb, layers, layer = 9, 16, 8, 4, 6, 3, 1
+    E = L + R
+    kv = mi.decode_f64(mi.draw("normal", 7011, T * L, 3.0), "f32").reshape(T, L)
+    kp = mi.decode_f64(mi.draw("normal", 7012, T * R, 3.0), "f32").reshape(T, R)
+    slots = np.array([5, -1, 0, 23, 7, 12, -3, 1, 18], np.int64)
+    storage = mi.permutation(7013, nb * layers * page * E).astype(np.uint8)   # sentinel bytes
+    strides = (layers * page * E, E, 1)
+    out = orc.cache_write_fp8(storage, layer * page * E, nb, page, strides, kv, kp, slots, 0.5)
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        base = layer * page * E + (s // page) * strides[0] + (s % page) * E
+        row = np.concatenate([kv[i], kp[i]]).astype(np.float32) / np.float32(0.5)
+        assert np.array_equal(out[base:base + E], orc.e4m3_code(row))
+        assert np.allclose(orc.e4m3_value(out[base:base + E]) * 0.5,
+                           np.concatenate([kv[i], kp[i]]), rtol=2 ** -4, atol=2 ** -10)
+    written = np.zeros(storage.size, bool)
+    for s in slots[slots >= 0]:
+        base = layer * page * E + (s // page) * strides[0] + (s % page) * E
+        written[base:base + E] = True
+    assert np.array_equal(out[~written], storage[~written])   # no bleed
+
+
+def test_fp8_decode_equals_decode_on_the_same_values():
+    # a cache whose values are exactly e4m3-representable, stored once as codes and once as
+    # float64 values: the fp8 decode with descale 1 is the plain decode of those values; an
+    # exact power-of-two descale_k scales the cache, descale_q scales the scores like the
+    # softmax scale
+    H, L, R, page, lens = 4, 8, 4, 4, [5, 9, 1]
+    E = L + R
+    nb = sum((n + page - 1) // page for n in lens) + 1
+    codes = mi.permutation(7021, 256 * ((nb * page * E) // 256 + 1))[: nb * page * E].astype(np.uint8)
+    codes = np.where((codes & 0x7F) == 0x7F, 0x38, codes).astype(np.uint8)       # no NaN codes
+    codes = np.where((codes >> 3 & 0xF) >= 11, codes & 0x87, codes).astype(np.uint8)   # keep |v| < 16
+    vals = orc.e4m3_value(codes)
+    perm = mi.permutation(7022, nb)
+    need = [(n + page - 1) // page for n in lens]
+    table = np.zeros((len(lens), max(need)), np.int64)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    q = mi.decode_f64(mi.draw("normal", 7023, len(lens) * H * E), "f32").reshape(len(lens), H, E)
+    args = (0, page, (page * E, E, 1), L, R, table, np.array(lens))
+    o1, l1 = orc.decode_fp8(q, codes, *args, 0.3, 1.0, 1.0)
+    o0, l0 = orc.decode(q, vals, *args, 0.3)
+    assert np.array_equal(o1, o0) and np.array_equal(l1, l0)
+    o4, _ = orc.decode_fp8(q, codes, *args, 0.3, 1.0, 4.0)
+    o4b, _ = orc.decode(q, vals * 4.0, *args, 0.3)
+    assert np.allclose(o4, o4b, rtol=1e-13, atol=1e-13)
+    o2, l2 = orc.decode_fp8(q, codes, *args, 0.3, 2.0, 1.0)
+    o2b, l2b = orc.decode(q, vals, *args, 0.6)
+    assert np.allclose(o2, o2b, rtol=1e-13, atol=1e-13) and np.allclose(l2, l2b, rtol=1e-13)
+
+
+def test_fp8_planted_mistakes_are_caught(monkeypatch):
+    # a wrong exponent bias, rounding by truncation, or a dropped descale must fail a pin
+    good_value = orc.e4m3_value
+    monkeypatch.setattr(orc, "e4m3_value", lambda c: good_value(c) * 2.0)   # bias off by one
+    with pytest.raises(AssertionError):
+        test_e4m3_values_are_the_formats()
+    monkeypatch.setattr(orc, "e4m3_value", good_value)
+    good_code = orc.e4m3_code
+
+    def truncating(x):
+        x = np.asarray(x, np.float32)
+        c = good_code(x)
+        over = np.abs(orc.e4m3_value(c)) > np.abs(x.astype(np.float64))
+        return np.where(over & ((c & 0x7F) > 0), c - 1, c).astype(np.uint8)
+
+    monkeypatch.setattr(orc, "e4m3_code", truncating)
+    with pytest.raises(AssertionError):
+        test_e4m3_round_trip_and_torch_agree()
+    monkeypatch.setattr(orc, "e4m3_code", good_code)
+    good_dec = orc.decode_fp8
+    monkeypatch.setattr(orc, "decode_fp8", lambda *a, **k: good_dec(*a[:10], 1.0, 1.0, *a[12:], **k))
+    with pytest.raises(AssertionError):
+        test_fp8_decode_equals_decode_on_the_same_values()
+    monkeypatch.setattr(orc, "decode_fp8", good_dec)
