@@ -158,6 +158,35 @@ mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank,
                                  int32_t num_splits);
 
+/* Step 3, fp8 cache - the cache write into an e4m3 cache ([vllm] concat_and_cache_mla
+ * with a quantized cache dtype and its scale).
+ *   cache [num_blocks, page, L+R] view of e4m3 codes, one byte per element (strides
+ *   count bytes), any stride(0) and storage offset; kv_c [T,L] and k_pe [T,R] in
+ *   src_dtype (MLA_F32 or MLA_BF16); slot_mapping: device int64 [num_tokens];
+ *   scale: device float [1], the cache scale.
+ *   For token i with s = slot_mapping[i] >= 0 the row s becomes the e4m3 codes of
+ *   float32(x) / scale (the division correctly rounded), rounded to nearest with
+ *   ties to even; finite values beyond 448 saturate to +-448, NaN stays NaN.
+ *   Padding slots, out-of-range slots and the untouched rows: as mla_cache_write. */
+mla_status mla_cache_write_fp8(mla_dtype src_dtype, mla_tensor cache, mla_tensor kv_c,
+                               mla_tensor k_pe, const int64_t* slot_mapping, int64_t num_tokens,
+                               const float* scale, void* stream);
+
+/* Step 4, fp8 cache - paged split-KV decode over an e4m3 cache ([vllm]
+ * flash_mla_with_kvcache_fp8 with descale_q and descale_k).
+ *   Arguments as mla_decode, except: cache holds e4m3 codes (one byte per element,
+ *   strides in bytes); every cache value is its code's value times *descale_k and
+ *   the query is q_cat times *descale_q (device floats [1]; NULL reads as 1).
+ *   o_lat_out and q_cat have `dtype`; the workspace is mla_decode's
+ *   (mla_decode_workspace_size). Results: as mla_decode over the dequantised
+ *   values. */
+mla_status mla_decode_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                          mla_tensor cache, const int32_t* block_table, int64_t block_table_stride,
+                          int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank,
+                          int32_t rope_dim, float softmax_scale, const float* descale_q,
+                          const float* descale_k, int32_t num_splits, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Step 4, prefill - causal attention of many queries per sequence over the same
  * paged cache ([memra] gate 1: pure prefill t_q == t_kv and the chunked shape
  * where the queries are a suffix of an already populated cache).

@@ -63,6 +63,9 @@ def lib() -> ctypes.CDLL:
             "mla_v_up": ([ctypes.c_int, T, T, T, P], ctypes.c_int),
             "mla_decode_noalloc": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, I32, P],
                                    ctypes.c_int),
+            "mla_cache_write_fp8": ([ctypes.c_int, T, T, T, P, I64, P, P], ctypes.c_int),
+            "mla_decode_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, P, P, I32, P, SZ, P],
+                               ctypes.c_int),
             "mla_device_error": ([P], ctypes.c_int),
             "mla_check_bounded_wait": ([ctypes.c_uint32, P], ctypes.c_int),
         }
@@ -148,6 +151,40 @@ def mla_cache_write(cache, kv_c, k_pe, slot_mapping, stream=None) -> None:
                                  slot_mapping.numel(), _stream(stream)))
 
 
+def _fp8_cache(cache):
+    """An e4m3 cache as a byte view (torch.float8_e4m3fn or uint8 storage of the codes)."""
+    import torch
+    if cache.dtype == torch.uint8:
+        return cache
+    if cache.dtype == getattr(torch, "float8_e4m3fn", None):
+        return cache.view(torch.uint8)
+    raise MlaError(MLA_ERR_INVALID_ARG, "an fp8 cache must be float8_e4m3fn or uint8 codes")
+
+
+def _f32_scalar(t, name):
+    import torch
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or t.numel() != 1 or not t.is_cuda:
+        raise MlaError(MLA_ERR_INVALID_ARG, f"{name} must be a device float32 tensor of one element")
+    return t.data_ptr()
+
+
+def mla_cache_write_fp8(cache, kv_c, k_pe, slot_mapping, scale, stream=None) -> None:
+    """Step 3 into an e4m3 cache: row s = e4m3([kv_c[i] | k_pe[i]] / scale) for s = slot_mapping[i] >= 0."""
+    import torch
+    if slot_mapping.dtype != torch.int64:
+        raise MlaError(MLA_ERR_INVALID_ARG, "slot_mapping must be int64")
+    if slot_mapping.numel() and not slot_mapping.is_contiguous():
+        raise MlaError(MLA_ERR_INVALID_ARG, "slot_mapping must be contiguous")
+    if kv_c.dtype != k_pe.dtype or kv_c.dtype not in (torch.float32, torch.bfloat16):
+        raise MlaError(MLA_ERR_INVALID_ARG, "kv_c and k_pe must both be float32 or both bfloat16")
+    src = MLA_F32 if kv_c.dtype == torch.float32 else MLA_BF16
+    _check(lib().mla_cache_write_fp8(src, as_mla_tensor(_fp8_cache(cache)), as_mla_tensor(kv_c),
+                                     as_mla_tensor(k_pe), _ptr(slot_mapping), slot_mapping.numel(),
+                                     _f32_scalar(scale, "scale"), _stream(stream)))
+
+
 def mla_decode_workspace_size(batch: int, num_heads: int, kv_lora_rank: int, num_splits: int = 0) -> int:
     return int(lib().mla_decode_workspace_size(batch, num_heads, kv_lora_rank, num_splits))
 
@@ -180,6 +217,29 @@ def mla_decode(o_lat_out, q_cat, cache, block_table, seq_lens, kv_lora_rank: int
                             seq_lens.data_ptr(), kv_lora_rank, rope_dim, softmax_scale, num_splits,
                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                             _stream(stream)))
+
+
+def mla_decode_fp8(o_lat_out, q_cat, cache, block_table, seq_lens, kv_lora_rank: int, rope_dim: int,
+                   softmax_scale: float, descale_q=None, descale_k=None, lse_out=None, num_splits: int = 0,
+                   workspace=None, stream=None) -> None:
+    """Step 4 over an e4m3 cache: mla_decode with cache values = code * descale_k and q * descale_q."""
+    import torch
+    _check_int32_table(block_table, seq_lens)
+    if lse_out is not None and (lse_out.dtype != torch.float32 or not lse_out.is_contiguous()):
+        raise MlaError(MLA_ERR_INVALID_ARG, "lse_out must be contiguous float32")
+    if o_lat_out.dtype != q_cat.dtype:
+        raise MlaError(MLA_ERR_INVALID_ARG, "o_lat_out and q_cat must share a dtype")
+    code = MLA_F32 if q_cat.dtype == torch.float32 else MLA_BF16
+    B, H = q_cat.shape[0], q_cat.shape[1]
+    need = mla_decode_workspace_size(B, H, kv_lora_rank, num_splits)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_cat.device)
+    _check(lib().mla_decode_fp8(code, as_mla_tensor(o_lat_out), _ptr(lse_out), as_mla_tensor(q_cat),
+                                as_mla_tensor(_fp8_cache(cache)), block_table.data_ptr(), block_table.stride(0),
+                                block_table.shape[1], seq_lens.data_ptr(), kv_lora_rank, rope_dim, softmax_scale,
+                                _f32_scalar(descale_q, "descale_q"), _f32_scalar(descale_k, "descale_k"),
+                                num_splits, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream(stream)))
 
 
 def mla_prefill_workspace_size(batch: int) -> int:

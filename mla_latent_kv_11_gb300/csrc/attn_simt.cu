@@ -19,6 +19,7 @@
 // softmax per head with warp shuffles and accumulates o_lat (each thread owns
 // 2 latent columns of every head of the group).
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 #include <algorithm>
@@ -36,6 +37,12 @@ constexpr int kThreads = 256;
 
 __device__ __forceinline__ float ld(const float* p) { return *p; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+// an fp8 cache holds e4m3 codes; their values are exact in float
+__device__ __forceinline__ float ld(const uint8_t* p) {
+  __nv_fp8_e4m3 v;
+  v.__x = *p;
+  return static_cast<float>(v);
+}
 __device__ __forceinline__ void st(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
@@ -255,17 +262,19 @@ __device__ inline SimtSmem simt_smem(unsigned char* raw, int E) {
   return s;
 }
 
-template <typename T>
+// K is the cache's element type (T, or e4m3 codes as uint8_t); the query is multiplied by
+// dq and every cache value by dk as they are staged (the dequantisation of an fp8 cache; 1 else).
+template <typename T, typename K>
 __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int64_t q_s_head,
                             int h0, int hn, int E, int L, const CacheView& cv,
                             const int32_t* __restrict__ bt_row, int k0, int k1, float scale,
-                            float (&acc)[kHeads][2]) {
+                            float (&acc)[kHeads][2], float dq = 1.f, float dk = 1.f) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = sm.pitch;
   __syncthreads();  // the previous segment's epilogue may still read m and l
   for (int i = tid; i < kHeads * E; i += kThreads) {
     const int h = i / E, e = i - h * E;
-    sm.q[h * P + e] = h < hn ? ld(q_row + (int64_t)(h0 + h) * q_s_head + e) : 0.f;
+    sm.q[h * P + e] = h < hn ? ld(q_row + (int64_t)(h0 + h) * q_s_head + e) * dq : 0.f;
   }
   if (tid < kHeads) {
     sm.m[tid] = -CUDART_INF_F;
@@ -273,7 +282,7 @@ __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int
   }
 #pragma unroll
   for (int h = 0; h < kHeads; ++h) acc[h][0] = acc[h][1] = 0.f;
-  const T* cache = static_cast<const T*>(cv.data);
+  const K* cache = static_cast<const K*>(cv.data);
   for (int kt = k0; kt < k1; kt += kKeys) {
     __syncthreads();
     // stage key rows kt .. kt+31 (rows past k1 are zero and masked below)
@@ -284,7 +293,7 @@ __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int
       if (t < k1) {
         const int blk = bt_row[t / cv.page];
         if (blk >= 0 && blk < cv.num_blocks)
-          v = ld(cache + (int64_t)blk * cv.s_blk + (int64_t)(t % cv.page) * cv.s_row + e);
+          v = ld(cache + (int64_t)blk * cv.s_blk + (int64_t)(t % cv.page) * cv.s_row + e) * dk;
         else if (e == 0)
           atomicOr(&g_attn_err, kErrDeviceData);
       }
@@ -337,15 +346,17 @@ __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int
   __syncthreads();
 }
 
-template <typename T>
+template <typename T, typename K>
 __global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
     T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
     const T* __restrict__ q, int64_t q_s0, int64_t q_s1, CacheView cv,
     const int32_t* __restrict__ block_table, int64_t bt_stride,
     const int32_t* __restrict__ seq_lens, int cap, int B, int H, int L, int R, float scale,
-    DecodeSched s) {
+    DecodeSched s, const float* __restrict__ descale_q, const float* __restrict__ descale_k) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   pdl_enter();
+  const float dq = descale_q != nullptr ? *descale_q : 1.f;
+  const float dk = descale_k != nullptr ? *descale_k : 1.f;
   const SimtSmem sm = simt_smem(smem_raw, L + R);
   const int w = blockIdx.x;
   const int t0 = s.unit_tile[w], t1 = s.unit_tile[w + 1];
@@ -366,8 +377,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
     const int len = min(max(seq_lens[b], 0), cap);
     const int k0 = (t - s.tile_prefix[b]) * kTile;
     const int k1 = min((seg_end - s.tile_prefix[b]) * kTile, len);
-    attend_rows<T>(sm, q + (int64_t)b * q_s0, q_s1, h0, hn, E, L, cv,
-                   block_table + (int64_t)b * bt_stride, k0, k1, scale, acc);
+    attend_rows<T, K>(sm, q + (int64_t)b * q_s0, q_s1, h0, hn, E, L, cv,
+                      block_table + (int64_t)b * bt_stride, k0, k1, scale, acc, dq, dk);
     const bool whole = s.npieces[b] == 1;
     const int slot = whole ? 0 : s.piece_base[b] + (w - s.first_unit[b]);
     for (int h = 0; h < hn; ++h) {
@@ -575,7 +586,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(
   int end = 0;
   if (i >= 0 && i < q_len) end = min(kv, max(0, kv - q_len + i + 1));
   float acc[kHeads][2];
-  attend_rows<T>(sm, q + (int64_t)r * q_s0, q_s1, h0, hn, L + R, L, cv,
+  attend_rows<T, T>(sm, q + (int64_t)r * q_s0, q_s1, h0, hn, L + R, L, cv,
                  block_table + (int64_t)b * bt_stride, 0, end, scale, acc);
   for (int h = 0; h < hn; ++h) {
     const float l = sm.l[h];
@@ -611,23 +622,33 @@ cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, con
                                const CacheView& cache, const int32_t* block_table,
                                int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t H,
                                int32_t L, int32_t R, float scale, const DecodeSched& s,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool fp8_cache, const float* descale_q, const float* descale_k) {
   const dim3 grid(s.units, (H + kHeads - 1) / kHeads);
   const long long cap_ll = (long long)max_blocks * cache.page;
   const int cap = (int)(cap_ll > INT32_MAX ? INT32_MAX : cap_ll);
   const size_t sm = simt_smem_bytes(L + R);
   if (dt == MLA_F32) {
-    allow_smem(decode_split_simt_kernel<float>, sm);
-    return launch_k(decode_split_simt_kernel<float>, grid, kThreads, sm, st,
+    if (fp8_cache) {
+      allow_smem(decode_split_simt_kernel<float, uint8_t>, sm);
+      return launch_k(decode_split_simt_kernel<float, uint8_t>, grid, kThreads, sm, st,
+          (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
+          block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
+    }
+    allow_smem(decode_split_simt_kernel<float, float>, sm);
+    return launch_k(decode_split_simt_kernel<float, float>, grid, kThreads, sm, st,
         (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
-        block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s);
-  } else {
-    allow_smem(decode_split_simt_kernel<__nv_bfloat16>, sm);
-    return launch_k(decode_split_simt_kernel<__nv_bfloat16>, grid, kThreads, sm, st,
-        (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
-        q.s1, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s);
+        block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
   }
-  return cudaGetLastError();
+  if (fp8_cache) {
+    allow_smem(decode_split_simt_kernel<__nv_bfloat16, uint8_t>, sm);
+    return launch_k(decode_split_simt_kernel<__nv_bfloat16, uint8_t>, grid, kThreads, sm, st,
+        (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
+        q.s1, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
+  }
+  allow_smem(decode_split_simt_kernel<__nv_bfloat16, __nv_bfloat16>, sm);
+  return launch_k(decode_split_simt_kernel<__nv_bfloat16, __nv_bfloat16>, grid, kThreads, sm, st,
+      (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
+      q.s1, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
 }
 
 cudaError_t launch_decode_combine(mla_dtype dt, const View3& o_lat, float* lse,

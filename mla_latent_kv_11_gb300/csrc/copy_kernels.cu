@@ -1,10 +1,14 @@
-// Step 2 (q concat) and step 3 (paged latent cache write): pure bit copies.
+// Step 2 (q concat) and step 3 (paged latent cache write): pure bit copies; and the
+// cache write into an fp8 (e4m3) cache, which converts instead of copying.
 //
 // Both move whole rows. When every row start and row length is a multiple of
 // 16 bytes the copy goes in 16-byte vectors (uint4), consecutive lanes on
 // consecutive vectors of a row; otherwise it falls back to element copies of
 // the same order. The element type never matters: bits are moved as integers, so NaN
 // payloads and signed zeros survive unchanged.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
 #include <cstdint>
 
 #include "mla_internal.h"
@@ -87,6 +91,76 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
   }
 }
 
+// e4m3 code of x / scale: the division correctly rounded in float32, then round to nearest
+// (ties to even), finite values beyond 448 saturating to +-448, NaN to NaN.
+__device__ __forceinline__ uint8_t e4m3_of(float x, float scale) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// Eight consecutive source values as floats (16-byte aligned: one 16-byte load for bf16, two for fp32).
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// cache[s/page, s%page, :] = e4m3([kv_c[i] | k_pe[i]] / scale) for every token with slot s >= 0.
+// Element strides (cache strides count bytes). vec8: every row start and L, R are multiples of 8
+// elements with the sources 16-byte and the cache rows 8-byte aligned, so a lane converts eight
+// values and stores them at once.
+template <typename T>
+__global__ void __launch_bounds__(256) cache_write_fp8_kernel(
+    uint8_t* __restrict__ cache, int64_t c_blk, int64_t c_row, int64_t num_rows, int32_t page,
+    const T* __restrict__ kv_c, int64_t k_s0, const T* __restrict__ k_pe, int64_t p_s0,
+    const int64_t* __restrict__ slots, int32_t L, int32_t R, int64_t T_, const float* __restrict__ scale_p,
+    RowSplit rs, int vec8) {
+  pdl_enter();
+  const float scale = *scale_p;
+  const int E = L + R;
+  int64_t tok, step;
+  int c0;
+  row_lane(rs, tok, step, c0);
+  for (; tok < T_; tok += step) {
+    const int64_t s = slots[tok];
+    if (s < 0) continue;  // padding
+    if (s >= num_rows) {  // would land outside the view: skip and record
+      if (c0 == 0) atomicOr(&g_copy_err, kErrDeviceData);
+      continue;
+    }
+    const int64_t blk = s / page, r = s - blk * page;
+    uint8_t* o = cache + blk * c_blk + r * c_row;
+    const T* kr = kv_c + tok * k_s0;
+    const T* pr = k_pe + tok * p_s0 - L;
+    if (vec8) {
+      for (int c = c0 * 8; c < E; c += rs.G * 8) {
+        float x[8];
+        load8(c < L ? kr + c : pr + c, x);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lo |= (uint32_t)e4m3_of(x[i], scale) << (8 * i);
+          hi |= (uint32_t)e4m3_of(x[4 + i], scale) << (8 * i);
+        }
+        *reinterpret_cast<uint2*>(o + c) = make_uint2(lo, hi);
+      }
+    } else {
+      for (int c = c0; c < E; c += rs.G) o[c] = e4m3_of(to_f(c < L ? kr[c] : pr[c]), scale);
+    }
+  }
+}
+
 RowSplit row_split(int64_t words) {
   RowSplit rs{32, 5};
   while (rs.G > 8 && rs.G / 2 >= words) {
@@ -164,6 +238,28 @@ cudaError_t launch_cache_write(mla_dtype dt, const View3& cache, const View3& kv
   return launch_k(cache_write_kernel<uint16_t>, grid_for(T, rs), 256, 0, st,
       (uint16_t*)cache.data, cache.s0, cache.s1, rows, page, (const uint16_t*)kv_c.data,
       kv_c.s0, (const uint16_t*)kp, k_pe.s0, slots, (int32_t)L, (int32_t)R, T, rs);
+}
+
+cudaError_t launch_cache_write_fp8(mla_dtype src_dt, const View3& cache, const View3& kv_c, const View3& k_pe,
+                                   int64_t L, int64_t R, const int64_t* slots, int64_t T, const float* scale,
+                                   cudaStream_t st) {
+  const int64_t rows = cache.n0 * cache.n1;
+  const int32_t page = (int32_t)cache.n1;
+  if (L + R >= INT32_MAX / 4) return cudaErrorInvalidValue;
+  auto al = [](const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+  const bool vec8 = L % 8 == 0 && R % 8 == 0 && al(cache.data, 8) && cache.s0 % 8 == 0 && cache.s1 % 8 == 0 &&
+                    al(kv_c.data, 16) && (R == 0 || al(k_pe.data, 16)) &&
+                    (kv_c.s0 * (src_dt == MLA_F32 ? 4 : 2)) % 16 == 0 &&
+                    (R == 0 || (k_pe.s0 * (src_dt == MLA_F32 ? 4 : 2)) % 16 == 0);
+  const RowSplit rs = row_split(vec8 ? (L + R) / 8 : L + R);
+  const void* kp = R == 0 ? kv_c.data : k_pe.data;
+  if (src_dt == MLA_F32)
+    return launch_k(cache_write_fp8_kernel<float>, grid_for(T, rs), 256, 0, st, (uint8_t*)cache.data, cache.s0,
+                    cache.s1, rows, page, (const float*)kv_c.data, kv_c.s0, (const float*)kp, k_pe.s0, slots,
+                    (int32_t)L, (int32_t)R, T, scale, rs, vec8 ? 1 : 0);
+  return launch_k(cache_write_fp8_kernel<__nv_bfloat16>, grid_for(T, rs), 256, 0, st, (uint8_t*)cache.data,
+                  cache.s0, cache.s1, rows, page, (const __nv_bfloat16*)kv_c.data, kv_c.s0,
+                  (const __nv_bfloat16*)kp, k_pe.s0, slots, (int32_t)L, (int32_t)R, T, scale, rs, vec8 ? 1 : 0);
 }
 
 unsigned copy_errors_read_clear() {

@@ -212,7 +212,8 @@ mla_status check_decode_args(mla_dtype dtype, const mla_tensor& o_lat_out, const
 
 mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, const int32_t* block_table,
                       int64_t block_table_stride, int32_t max_blocks, const int32_t* seq_lens, float softmax_scale,
-                      void* scratch, const DecodeWsLayout& lay, cudaStream_t st) {
+                      void* scratch, const DecodeWsLayout& lay, cudaStream_t st, bool fp8_cache,
+                      const float* descale_q, const float* descale_k) {
   const DecodeSched s = decode_sched_from_ws(scratch, lay, (int32_t)dc.B, dc.units);
   const int32_t B = (int32_t)dc.B, H = (int32_t)dc.H, L = (int32_t)dc.L, R = (int32_t)dc.R;
   MLA_TRY(cuda_status(launch_decode_schedule(seq_lens, B, max_blocks, dc.cv.page, s, st), "mla_decode schedule"));
@@ -222,7 +223,8 @@ mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, con
                         "mla_decode split kernel (tensor cores)"));
   } else {
     MLA_TRY(cuda_status(launch_decode_simt(dtype, dc.ov, lse_out, dc.qv, dc.cv, block_table, block_table_stride,
-                                           max_blocks, seq_lens, B, H, L, R, softmax_scale, s, st),
+                                           max_blocks, seq_lens, B, H, L, R, softmax_scale, s, st, fp8_cache,
+                                           descale_q, descale_k),
                         "mla_decode split kernel"));
   }
   return cuda_status(launch_decode_combine(dtype, dc.ov, lse_out, seq_lens, B, H, L, s, st), "mla_decode combine");
@@ -349,6 +351,51 @@ mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla
     return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   return run_decode(dtype, dc, lse_out, block_table, block_table_stride, max_blocks, seq_lens, softmax_scale,
                     workspace, lay, (cudaStream_t)stream);
+}
+
+mla_status mla_cache_write_fp8(mla_dtype src_dtype, mla_tensor cache, mla_tensor kv_c, mla_tensor k_pe,
+                               const int64_t* slot_mapping, int64_t num_tokens, const float* scale,
+                               void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(src_dtype));
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens < 0");
+  MLA_TRY(check_view(kv_c, 2, "kv_c"));
+  MLA_TRY(check_view(k_pe, 2, "k_pe"));
+  const int64_t L = kv_c.shape[1], R = k_pe.shape[1];
+  MLA_TRY(check_cache(cache, L + R, "cache"));
+  if (kv_c.shape[0] != num_tokens || k_pe.shape[0] != num_tokens)
+    return fail(MLA_ERR_INVALID_ARG, "kv_c/k_pe rows (%lld/%lld) != num_tokens %lld",
+                (long long)kv_c.shape[0], (long long)k_pe.shape[0], (long long)num_tokens);
+  if (num_tokens == 0) return MLA_OK;
+  if (slot_mapping == nullptr || scale == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "slot_mapping and scale must be non-null");
+  View3 kc{kv_c.data, kv_c.shape[0], 1, kv_c.shape[1], kv_c.stride[0], 0, 1};
+  View3 kp{k_pe.data, k_pe.shape[0], 1, k_pe.shape[1], k_pe.stride[0], 0, 1};
+  return cuda_status(launch_cache_write_fp8(src_dtype, view3(cache), kc, kp, L, R, slot_mapping, num_tokens, scale,
+                                            (cudaStream_t)stream),
+                     "mla_cache_write_fp8");
+}
+
+mla_status mla_decode_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                          mla_tensor cache, const int32_t* block_table, int64_t block_table_stride,
+                          int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim,
+                          float softmax_scale, const float* descale_q, const float* descale_k,
+                          int32_t num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  DecodeCall dc;
+  MLA_TRY(check_decode_args(dtype, o_lat_out, q_cat, cache, block_table, block_table_stride, max_blocks,
+                            seq_lens, kv_lora_rank, rope_dim, softmax_scale, num_splits, &dc));
+  if (dc.empty) return MLA_OK;
+  dc.tc = false;   // the e4m3 cache is read by the general kernel
+  dc.units = decode_units(num_splits);
+  const DecodeWsLayout lay = decode_ws_layout(dc.B, dc.H, dc.L, decode_units(num_splits));
+  if (workspace == nullptr || workspace_bytes < lay.total)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes,
+                lay.total);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  return run_decode(dtype, dc, lse_out, block_table, block_table_stride, max_blocks, seq_lens, softmax_scale,
+                    workspace, lay, (cudaStream_t)stream, true, descale_q, descale_k);
 }
 
 size_t mla_prefill_workspace_size(int32_t batch) {

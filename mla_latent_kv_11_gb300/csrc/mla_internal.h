@@ -112,11 +112,19 @@ cudaError_t launch_bmm_tc(const View3& out, const View3& a, const View3& b, cuda
 
 cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
                                    int32_t page, const DecodeSched& s, cudaStream_t st);
+// fp8_cache: the cache holds e4m3 codes (one byte each), read as value * (*descale_k) with the
+// query scaled by *descale_q (null pointers read as 1).
 cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
                                const CacheView& cache, const int32_t* block_table,
                                int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t H,
                                int32_t L, int32_t R, float scale, const DecodeSched& s,
-                               cudaStream_t st);
+                               cudaStream_t st, bool fp8_cache = false, const float* descale_q = nullptr,
+                               const float* descale_k = nullptr);
+// e4m3 cache write: codes of x / (*scale) (float32, correctly rounded), round to nearest even,
+// saturating; src_dt is kv_c's and k_pe's element type.
+cudaError_t launch_cache_write_fp8(mla_dtype src_dt, const View3& cache, const View3& kv_c, const View3& k_pe,
+                                   int64_t L, int64_t R, const int64_t* slots, int64_t T, const float* scale,
+                                   cudaStream_t st);
 cudaError_t launch_decode_combine(mla_dtype dt, const View3& o_lat, float* lse,
                                   const int32_t* seq_lens, int32_t B, int32_t H, int32_t L,
                                   const DecodeSched& s, cudaStream_t st);
@@ -160,9 +168,11 @@ mla_status check_decode_args(mla_dtype dtype, const mla_tensor& o_lat_out, const
                              int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim,
                              float softmax_scale, int32_t num_splits, DecodeCall* out);
 // Schedule, split kernel and combine of a validated decode, with its scratch laid out by `lay`.
+// fp8_cache: the cache holds e4m3 codes read as value * (*descale_k), the query scaled by *descale_q.
 mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, const int32_t* block_table,
                       int64_t block_table_stride, int32_t max_blocks, const int32_t* seq_lens, float softmax_scale,
-                      void* scratch, const DecodeWsLayout& lay, cudaStream_t st);
+                      void* scratch, const DecodeWsLayout& lay, cudaStream_t st, bool fp8_cache = false,
+                      const float* descale_q = nullptr, const float* descale_k = nullptr);
 
 // Set (or clear, with MLA_OK) the calling thread's mla_last_error() message.
 mla_status report_status(mla_status st, const char* fmt, ...);
