@@ -158,6 +158,19 @@ mla_status mla_decode(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank,
                                  int32_t num_splits);
 
+/* Steps 2 and 3 in one launch - the q concat and the cache write of the same
+ * decode step (the fused pre-attention of the vllm.cpp and memra pages' step
+ * order: the new rows' [c_kv | k_pe] go into the cache while the query's rope
+ * columns join q_cat).
+ *   Arguments: those of mla_concat_q followed by those of mla_cache_write (one
+ *   dtype for all tensors). Results, errors and the in-place nope case are
+ *   exactly theirs; when either part cannot move 16-byte words the two run as
+ *   two launches. */
+mla_status mla_concat_q_cache_write(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope,
+                                    mla_tensor rope, mla_tensor cache, mla_tensor kv_c,
+                                    mla_tensor k_pe, const int64_t* slot_mapping,
+                                    int64_t num_tokens, void* stream);
+
 /* Step 3, fp8 cache - the cache write into an e4m3 cache ([vllm] concat_and_cache_mla
  * with a quantized cache dtype and its scale).
  *   cache [num_blocks, page, L+R] view of e4m3 codes, one byte per element (strides

@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
             "mla_decode_noalloc": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, I32, P],
                                    ctypes.c_int),
             "mla_cache_write_fp8": ([ctypes.c_int, T, T, T, P, I64, P, P], ctypes.c_int),
+            "mla_concat_q_cache_write": ([ctypes.c_int, T, T, T, T, T, T, P, I64, P], ctypes.c_int),
             "mla_decode_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, P, P, I32, P, SZ, P],
                                ctypes.c_int),
             "mla_device_error": ([P], ctypes.c_int),
@@ -183,6 +184,20 @@ def mla_cache_write_fp8(cache, kv_c, k_pe, slot_mapping, scale, stream=None) -> 
     _check(lib().mla_cache_write_fp8(src, as_mla_tensor(_fp8_cache(cache)), as_mla_tensor(kv_c),
                                      as_mla_tensor(k_pe), _ptr(slot_mapping), slot_mapping.numel(),
                                      _f32_scalar(scale, "scale"), _stream(stream)))
+
+
+def mla_concat_q_cache_write(q_cat_out, nope, rope, cache, kv_c, k_pe, slot_mapping, stream=None) -> None:
+    """Steps 2 and 3 in one launch: mla_concat_q(q_cat_out, nope, rope) and
+    mla_cache_write(cache, kv_c, k_pe, slot_mapping)."""
+    import torch
+    if slot_mapping.dtype != torch.int64:
+        raise MlaError(MLA_ERR_INVALID_ARG, "slot_mapping must be int64")
+    if slot_mapping.numel() and not slot_mapping.is_contiguous():
+        raise MlaError(MLA_ERR_INVALID_ARG, "slot_mapping must be contiguous")
+    _check(lib().mla_concat_q_cache_write(_dtype_code(q_cat_out, nope, rope, cache, kv_c, k_pe),
+                                          as_mla_tensor(q_cat_out), as_mla_tensor(nope), as_mla_tensor(rope),
+                                          as_mla_tensor(cache), as_mla_tensor(kv_c), as_mla_tensor(k_pe),
+                                          _ptr(slot_mapping), slot_mapping.numel(), _stream(stream)))
 
 
 def mla_decode_workspace_size(batch: int, num_heads: int, kv_lora_rank: int, num_splits: int = 0) -> int:

@@ -1049,7 +1049,10 @@ bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint
 bool tc_attention_supported(mla_dtype dt, int H, int L, int R, bool decode, const CacheView& cv,
                             const View3& q, const View3& o) {
   if (dt != MLA_BF16 || L != 512 || (R != 0 && R != 64)) return false;
-  if (decode ? H != 128 : (H != 128 && H != 64)) return false;
+  // 128 heads fill the 128-row tile; 64 heads use half of it in decode (one token per
+  // sequence: the other rows are masked) and two tokens per tile in prefill
+  (void)decode;
+  if (H != 128 && H != 64) return false;
   const int page = cv.page;
   if (!(page % 64 == 0 || (64 % page == 0 && page % 8 == 0))) return false;
   auto al16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };

@@ -172,6 +172,75 @@ RowSplit row_split(int64_t words) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// The q concat and the cache write of the same step in one launch: blocks [0, q_blocks) run
+// the concat over q rows, the remaining blocks the cache write over tokens, each part with its
+// own lane-group split and striding over its own block range. Both parts move 16-byte words.
+struct ConcatArgs {
+  uint4* out;
+  int64_t o_s0, o_s1;
+  const uint4* nope;
+  int64_t n_s0, n_s1;
+  const uint4* rope;
+  int64_t r_s0, r_s1;
+  int32_t H, Lw, Rw, rows;
+  RowSplit rs;
+};
+struct CacheArgs {
+  uint4* cache;
+  int64_t c_blk, c_row, num_rows;
+  int32_t page;
+  const uint4* kv_c;
+  int64_t k_s0;
+  const uint4* k_pe;
+  int64_t p_s0;
+  const int64_t* slots;
+  int32_t Lw, Rw;
+  int64_t T;
+  RowSplit rs;
+};
+
+__global__ void __launch_bounds__(256) concat_cache_kernel(ConcatArgs a, CacheArgs c, int q_blocks) {
+  pdl_enter();
+  const bool q_part = (int)blockIdx.x < q_blocks;
+  const int part_block = q_part ? blockIdx.x : blockIdx.x - q_blocks;
+  const int part_blocks = q_part ? q_blocks : gridDim.x - q_blocks;
+  const RowSplit rs = q_part ? a.rs : c.rs;
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = (part_block * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)part_blocks * blockDim.x) >> 5;
+  const int per_warp = 32 >> rs.shift;
+  const int c0 = lane & (rs.G - 1);
+  const int64_t step = nwarps * per_warp;
+  int64_t r = gwarp * per_warp + (lane >> rs.shift);
+  if (q_part) {
+    const int Ew = a.Lw + a.Rw;
+    for (; r < a.rows; r += step) {
+      const int t = (int)r / a.H, h = (int)r - t * a.H;
+      uint4* o = a.out + t * a.o_s0 + h * a.o_s1;
+      const uint4* nr = a.nope + t * a.n_s0 + h * a.n_s1;
+      const uint4* rr = a.rope + t * a.r_s0 + h * a.r_s1 - a.Lw;
+      for (int cc = c0; cc < Ew; cc += rs.G) o[cc] = cc < a.Lw ? nr[cc] : rr[cc];
+    }
+  } else {
+    const int Ew = c.Lw + c.Rw;
+    for (; r < c.T; r += step) {
+      const int64_t sl = c.slots[r];
+      if (sl < 0) continue;
+      if (sl >= c.num_rows) {
+        if (c0 == 0) atomicOr(&g_copy_err, kErrDeviceData);
+        continue;
+      }
+      const int64_t blk = sl / c.page, row = sl - blk * c.page;
+      uint4* o = c.cache + blk * c.c_blk + row * c.c_row;
+      const uint4* kr = c.kv_c + r * c.k_s0;
+      const uint4* pr = c.k_pe + r * c.p_s0 - c.Lw;
+      for (int cc = c0; cc < Ew; cc += rs.G) o[cc] = cc < c.Lw ? kr[cc] : pr[cc];
+    }
+  }
+}
+
+
+
 // Enough 256-thread blocks for one row group per row, capped at 16 blocks per SM (the
 // kernels stride over the rest).
 int grid_for(int64_t rows, const RowSplit& rs) {
@@ -260,6 +329,60 @@ cudaError_t launch_cache_write_fp8(mla_dtype src_dt, const View3& cache, const V
   return launch_k(cache_write_fp8_kernel<__nv_bfloat16>, grid_for(T, rs), 256, 0, st, (uint8_t*)cache.data,
                   cache.s0, cache.s1, rows, page, (const __nv_bfloat16*)kv_c.data, kv_c.s0,
                   (const __nv_bfloat16*)kp, k_pe.s0, slots, (int32_t)L, (int32_t)R, T, scale, rs, vec8 ? 1 : 0);
+}
+
+cudaError_t launch_concat_cache(mla_dtype dt, const View3& out, const View3& nope, const View3& rope,
+                                const View3& cache, const View3& kv_c, const View3& k_pe, int64_t L, int64_t R,
+                                const int64_t* slots, int64_t T, cudaStream_t st) {
+  const int64_t es = dt == MLA_F32 ? 4 : 2;
+  const int64_t per = 16 / es;
+  const int64_t Tq = out.n0, H = out.n1, Lq = nope.n2, Rq = rope.n2;
+  const int64_t qrows = Tq * H;
+  const bool q_vec = aligned16(out.data) && (Lq == 0 || aligned16(nope.data)) && (Rq == 0 || aligned16(rope.data)) &&
+                     Lq % per == 0 && Rq % per == 0 && out.s0 % per == 0 && out.s1 % per == 0 &&
+                     nope.s0 % per == 0 && nope.s1 % per == 0 && (Rq == 0 || (rope.s0 % per == 0 && rope.s1 % per == 0));
+  const bool c_vec = aligned16(cache.data) && aligned16(kv_c.data) && (R == 0 || aligned16(k_pe.data)) &&
+                     L % per == 0 && R % per == 0 && cache.s0 % per == 0 && cache.s1 % per == 0 &&
+                     kv_c.s0 % per == 0 && (R == 0 || k_pe.s0 % per == 0);
+  if (!q_vec || !c_vec || qrows >= INT32_MAX || qrows == 0 || T == 0) {
+    // one of the two cannot take 16-byte words (or is empty): two launches, same results
+    cudaError_t e = cudaSuccess;
+    if (qrows > 0) e = launch_concat_q(dt, out, nope, rope, st);
+    if (e == cudaSuccess && T > 0) e = launch_cache_write(dt, cache, kv_c, k_pe, L, R, slots, T, st);
+    return e;
+  }
+  ConcatArgs a;
+  a.out = (uint4*)out.data;
+  a.o_s0 = out.s0 / per;
+  a.o_s1 = out.s1 / per;
+  a.nope = (const uint4*)(Lq == 0 ? out.data : nope.data);
+  a.n_s0 = nope.s0 / per;
+  a.n_s1 = nope.s1 / per;
+  a.rope = (const uint4*)(Rq == 0 ? out.data : rope.data);
+  a.r_s0 = rope.s0 / per;
+  a.r_s1 = rope.s1 / per;
+  a.H = (int32_t)H;
+  a.Lw = (int32_t)(Lq / per);
+  a.Rw = (int32_t)(Rq / per);
+  a.rows = (int32_t)qrows;
+  a.rs = row_split((Lq + Rq) / per);
+  CacheArgs c;
+  c.cache = (uint4*)cache.data;
+  c.c_blk = cache.s0 / per;
+  c.c_row = cache.s1 / per;
+  c.num_rows = cache.n0 * cache.n1;
+  c.page = (int32_t)cache.n1;
+  c.kv_c = (const uint4*)kv_c.data;
+  c.k_s0 = kv_c.s0 / per;
+  c.k_pe = (const uint4*)(R == 0 ? kv_c.data : k_pe.data);
+  c.p_s0 = k_pe.s0 / per;
+  c.slots = slots;
+  c.Lw = (int32_t)(L / per);
+  c.Rw = (int32_t)(R / per);
+  c.T = T;
+  c.rs = row_split((L + R) / per);
+  const int qb = grid_for(qrows, a.rs), cb = grid_for(T, c.rs);
+  return launch_k(concat_cache_kernel, qb + cb, 256, 0, st, a, c, qb);
 }
 
 unsigned copy_errors_read_clear() {

@@ -168,6 +168,69 @@ int32_t decode_units(int32_t num_splits) {
   return 2 * device_sm_count();
 }
 
+// The argument checks of the q concat; on MLA_OK *out holds the views to copy (when nope is
+// q_cat_out's own first L columns, only the rope columns remain to move).
+mla_status plan_concat(mla_dtype dtype, const mla_tensor& q_cat_out, const mla_tensor& nope,
+                       const mla_tensor& rope, ConcatPlan* out) {
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat_out, 3, "q_cat_out"));
+  MLA_TRY(check_view(nope, 3, "nope"));
+  MLA_TRY(check_view(rope, 3, "rope"));
+  const int64_t T = q_cat_out.shape[0], H = q_cat_out.shape[1];
+  if (nope.shape[0] != T || nope.shape[1] != H)
+    return fail(MLA_ERR_INVALID_ARG, "nope [%lld,%lld,.] does not match q_cat_out [%lld,%lld,.]",
+                (long long)nope.shape[0], (long long)nope.shape[1], (long long)T, (long long)H);
+  if (rope.shape[0] != T || (rope.shape[1] != H && rope.shape[1] != 1))
+    return fail(MLA_ERR_INVALID_ARG, "rope must be [T,H,R] or [T,1,R]");
+  if (nope.shape[2] + rope.shape[2] != q_cat_out.shape[2])
+    return fail(MLA_ERR_INVALID_ARG, "q_cat_out width %lld != L + R = %lld",
+                (long long)q_cat_out.shape[2], (long long)(nope.shape[2] + rope.shape[2]));
+  out->empty = numel(q_cat_out) == 0;
+  if (out->empty) return MLA_OK;
+  View3 r = view3(rope);
+  if (rope.shape[1] == 1) r.s1 = 0;  // one rope head broadcast to every head
+  r.n1 = H;
+  View3 o = view3(q_cat_out), nv = view3(nope);
+  if (nope.data == q_cat_out.data && nope.stride[0] == q_cat_out.stride[0] &&
+      nope.stride[1] == q_cat_out.stride[1] && nope.stride[2] == q_cat_out.stride[2]) {
+    // nope is q_cat_out's own first L columns (the absorb wrote q_lat in place): they are
+    // already there, only the rope columns move
+    const size_t es = dtype == MLA_F32 ? 4 : 2;
+    o.data = static_cast<char*>(o.data) + es * (size_t)nope.shape[2];
+    o.n2 = rope.shape[2];
+    nv.n2 = 0;
+    if (rope.shape[2] == 0) out->empty = true;
+  }
+  out->out = o;
+  out->nope = nv;
+  out->rope = r;
+  return MLA_OK;
+}
+
+// The argument checks of the cache write; on MLA_OK *out holds the views.
+mla_status plan_cache_write(mla_dtype dtype, const mla_tensor& cache, const mla_tensor& kv_c,
+                            const mla_tensor& k_pe, const int64_t* slot_mapping, int64_t num_tokens,
+                            WritePlan* out) {
+  MLA_TRY(check_dtype(dtype));
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens < 0");
+  MLA_TRY(check_view(kv_c, 2, "kv_c"));
+  MLA_TRY(check_view(k_pe, 2, "k_pe"));
+  const int64_t L = kv_c.shape[1], R = k_pe.shape[1];
+  MLA_TRY(check_cache(cache, L + R, "cache"));
+  if (kv_c.shape[0] != num_tokens || k_pe.shape[0] != num_tokens)
+    return fail(MLA_ERR_INVALID_ARG, "kv_c/k_pe rows (%lld/%lld) != num_tokens %lld",
+                (long long)kv_c.shape[0], (long long)k_pe.shape[0], (long long)num_tokens);
+  out->empty = num_tokens == 0;
+  if (out->empty) return MLA_OK;
+  if (slot_mapping == nullptr) return fail(MLA_ERR_INVALID_ARG, "slot_mapping is null");
+  out->L = L;
+  out->R = R;
+  out->cache = view3(cache);
+  out->kv_c = View3{kv_c.data, kv_c.shape[0], 1, kv_c.shape[1], kv_c.stride[0], 0, 1};
+  out->k_pe = View3{k_pe.data, k_pe.shape[0], 1, k_pe.shape[1], k_pe.stride[0], 0, 1};
+  return MLA_OK;
+}
+
 mla_status check_decode_args(mla_dtype dtype, const mla_tensor& o_lat_out, const mla_tensor& q_cat,
                              const mla_tensor& cache, const int32_t* block_table, int64_t block_table_stride,
                              int32_t max_blocks, const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim,
@@ -275,55 +338,40 @@ mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tenso
 mla_status mla_concat_q(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope, mla_tensor rope,
                         void* stream) {
   g_msg[0] = 0;
-  MLA_TRY(check_dtype(dtype));
-  MLA_TRY(check_view(q_cat_out, 3, "q_cat_out"));
-  MLA_TRY(check_view(nope, 3, "nope"));
-  MLA_TRY(check_view(rope, 3, "rope"));
-  const int64_t T = q_cat_out.shape[0], H = q_cat_out.shape[1];
-  if (nope.shape[0] != T || nope.shape[1] != H)
-    return fail(MLA_ERR_INVALID_ARG, "nope [%lld,%lld,.] does not match q_cat_out [%lld,%lld,.]",
-                (long long)nope.shape[0], (long long)nope.shape[1], (long long)T, (long long)H);
-  if (rope.shape[0] != T || (rope.shape[1] != H && rope.shape[1] != 1))
-    return fail(MLA_ERR_INVALID_ARG, "rope must be [T,H,R] or [T,1,R]");
-  if (nope.shape[2] + rope.shape[2] != q_cat_out.shape[2])
-    return fail(MLA_ERR_INVALID_ARG, "q_cat_out width %lld != L + R = %lld",
-                (long long)q_cat_out.shape[2], (long long)(nope.shape[2] + rope.shape[2]));
-  if (numel(q_cat_out) == 0) return MLA_OK;
-  View3 r = view3(rope);
-  if (rope.shape[1] == 1) r.s1 = 0;  // one rope head broadcast to every head
-  r.n1 = H;
-  View3 out = view3(q_cat_out), nv = view3(nope);
-  if (nope.data == q_cat_out.data && nope.stride[0] == q_cat_out.stride[0] &&
-      nope.stride[1] == q_cat_out.stride[1] && nope.stride[2] == q_cat_out.stride[2]) {
-    // nope is q_cat_out's own first L columns (the absorb wrote q_lat in place): they are
-    // already there, only the rope columns move
-    const size_t es = dtype == MLA_F32 ? 4 : 2;
-    out.data = static_cast<char*>(out.data) + es * (size_t)nope.shape[2];
-    out.n2 = rope.shape[2];
-    nv.n2 = 0;
-    if (rope.shape[2] == 0) return MLA_OK;
-  }
-  return cuda_status(launch_concat_q(dtype, out, nv, r, (cudaStream_t)stream), "mla_concat_q");
+  ConcatPlan cp;
+  MLA_TRY(plan_concat(dtype, q_cat_out, nope, rope, &cp));
+  if (cp.empty) return MLA_OK;
+  return cuda_status(launch_concat_q(dtype, cp.out, cp.nope, cp.rope, (cudaStream_t)stream), "mla_concat_q");
 }
 
 mla_status mla_cache_write(mla_dtype dtype, mla_tensor cache, mla_tensor kv_c, mla_tensor k_pe,
                            const int64_t* slot_mapping, int64_t num_tokens, void* stream) {
   g_msg[0] = 0;
-  MLA_TRY(check_dtype(dtype));
-  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens < 0");
-  MLA_TRY(check_view(kv_c, 2, "kv_c"));
-  MLA_TRY(check_view(k_pe, 2, "k_pe"));
-  const int64_t L = kv_c.shape[1], R = k_pe.shape[1];
-  MLA_TRY(check_cache(cache, L + R, "cache"));
-  if (kv_c.shape[0] != num_tokens || k_pe.shape[0] != num_tokens)
-    return fail(MLA_ERR_INVALID_ARG, "kv_c/k_pe rows (%lld/%lld) != num_tokens %lld",
-                (long long)kv_c.shape[0], (long long)k_pe.shape[0], (long long)num_tokens);
-  if (num_tokens == 0) return MLA_OK;
-  if (slot_mapping == nullptr) return fail(MLA_ERR_INVALID_ARG, "slot_mapping is null");
-  View3 kc{kv_c.data, kv_c.shape[0], 1, kv_c.shape[1], kv_c.stride[0], 0, 1};
-  View3 kp{k_pe.data, k_pe.shape[0], 1, k_pe.shape[1], k_pe.stride[0], 0, 1};
-  return cuda_status(launch_cache_write(dtype, view3(cache), kc, kp, L, R, slot_mapping, num_tokens,
+  WritePlan wp;
+  MLA_TRY(plan_cache_write(dtype, cache, kv_c, k_pe, slot_mapping, num_tokens, &wp));
+  if (wp.empty) return MLA_OK;
+  return cuda_status(launch_cache_write(dtype, wp.cache, wp.kv_c, wp.k_pe, wp.L, wp.R, slot_mapping, num_tokens,
                                         (cudaStream_t)stream), "mla_cache_write");
+}
+
+mla_status mla_concat_q_cache_write(mla_dtype dtype, mla_tensor q_cat_out, mla_tensor nope, mla_tensor rope,
+                                    mla_tensor cache, mla_tensor kv_c, mla_tensor k_pe,
+                                    const int64_t* slot_mapping, int64_t num_tokens, void* stream) {
+  g_msg[0] = 0;
+  ConcatPlan cp;
+  MLA_TRY(plan_concat(dtype, q_cat_out, nope, rope, &cp));
+  WritePlan wp;
+  MLA_TRY(plan_cache_write(dtype, cache, kv_c, k_pe, slot_mapping, num_tokens, &wp));
+  if (cp.empty && wp.empty) return MLA_OK;
+  View3 out = cp.out, nv = cp.nope, rv = cp.rope;
+  if (cp.empty) {   // nothing to concatenate: an empty q part
+    out.n0 = 0;
+    nv.n2 = 0;
+    rv.n2 = 0;
+  }
+  return cuda_status(launch_concat_cache(dtype, out, nv, rv, wp.cache, wp.kv_c, wp.k_pe, wp.L, wp.R, slot_mapping,
+                                         wp.empty ? 0 : num_tokens, (cudaStream_t)stream),
+                     "mla_concat_q_cache_write");
 }
 
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank,

@@ -134,8 +134,8 @@ cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, co
                                 const int32_t* kv_lens, int32_t B, int32_t T, int32_t H,
                                 int32_t L, int32_t R, float scale, cudaStream_t st);
 
-// Tensor-core attention (attn_tc.cu): bf16, L = 512, R in {0, 64}, 16-byte
-// aligned views; decode needs H = 128, prefill H in {64, 128}.
+// Tensor-core attention (attn_tc.cu): bf16, L = 512, R in {0, 64}, H in {64, 128}, 16-byte
+// aligned views.
 bool tc_attention_supported(mla_dtype dt, int H, int L, int R, bool decode, const CacheView& cv,
                             const View3& q, const View3& o);
 int tc_decode_units(int num_splits);
@@ -148,6 +148,26 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
                               const int32_t* cu_q, const int32_t* kv_lens, int32_t B, int32_t H,
                               int32_t L, int32_t R, float scale, int32_t* item_prefix,
                               cudaStream_t st);
+
+// Validated views of a q concat and of a cache write (mla_api.cu).
+struct ConcatPlan {
+  bool empty = true;
+  View3 out{}, nope{}, rope{};
+};
+struct WritePlan {
+  bool empty = true;
+  int64_t L = 0, R = 0;
+  View3 cache{}, kv_c{}, k_pe{};
+};
+mla_status plan_concat(mla_dtype dtype, const mla_tensor& q_cat_out, const mla_tensor& nope,
+                       const mla_tensor& rope, ConcatPlan* out);
+mla_status plan_cache_write(mla_dtype dtype, const mla_tensor& cache, const mla_tensor& kv_c,
+                            const mla_tensor& k_pe, const int64_t* slot_mapping, int64_t num_tokens,
+                            WritePlan* out);
+// The q concat and the cache write in one launch when both take 16-byte words, else two.
+cudaError_t launch_concat_cache(mla_dtype dt, const View3& out, const View3& nope, const View3& rope,
+                                const View3& cache, const View3& kv_c, const View3& k_pe, int64_t L, int64_t R,
+                                const int64_t* slots, int64_t T, cudaStream_t st);
 
 // Work units of the general (CUDA-core) split-KV decode: num_splits, or two per SM.
 int32_t decode_units(int32_t num_splits);

@@ -162,3 +162,60 @@ def test_absorb_into_q_cat_then_concat_in_place(mla, dtype, case):
     mla.mla_absorb_q(sep, to_dev(qn, dtype).transpose(0, 1), to_dev(w, dtype))
     torch.cuda.synchronize()
     assert np.array_equal(np.transpose(to_host_bits(sep), (1, 0, 2)), got_bits[:, :, :L])
+
+
+@pytest.mark.parametrize("in_place", [False, True], ids=["separate_nope", "absorbed_in_place"])
+def test_concat_and_cache_write_in_one_launch(mla, in_place):
+    # Steps 2 and 3 together: the q_cat rows and the cache rows are the oracle's gathers,
+    # bit for bit, and the neighbouring layers of the unified cache keep their sentinel.
+    import torch
+    w = mi.write_concat_workload()
+    nb, page, E, n_layers, layer = w.num_blocks, w.page, w.entry, w.n_layers, w.layer
+    N, B, L = w.q_nope_storage.shape
+    R = w.q_pe.shape[2]
+    store = to_dev(w.q_nope_storage, "bf16")
+    nope = store.as_strided((B, N, L), (L, B * L, 1))
+    out = poisoned((B, N, L + R), "bf16")
+    if in_place:
+        out[:, :, :L].copy_(nope)
+        nope = out[:, :, :L]
+    big = _unified(nb, n_layers, page, E)
+    flat = big.view(-1)
+    view = flat.as_strided((nb, page, E), (n_layers * page * E, E, 1), layer * page * E)
+    mla.mla_concat_q_cache_write(out, nope, to_dev(w.q_pe, "bf16"), view, to_dev(w.kv_c, "bf16"),
+                                 to_dev(w.k_pe, "bf16"), torch.from_numpy(w.slots).cuda())
+    mla.mla_device_error()
+    nope_h = orc.strided_view(w.q_nope_storage.reshape(-1), 0, (B, N, L), (L, B * L, 1))
+    assert np.array_equal(to_host_bits(out), orc.concat_q(np.ascontiguousarray(nope_h), w.q_pe))
+    want = orc.cache_write(np.full(nb * n_layers * page * E, 0x1234, np.uint16), layer * page * E, nb,
+                           page, (n_layers * page * E, E, 1), w.kv_c, w.k_pe, w.slots)
+    assert np.array_equal(to_host_bits(flat), want)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", ["odd_widths", "no_tokens", "no_rows"])
+def test_concat_and_cache_write_in_one_launch_edges(mla, dtype, case):
+    # Odd widths take the element path (two launches inside the call); an empty half leaves
+    # only the other one to run.
+    import torch
+    T, H, L, R, Hr = (7, 5, 13, 3, 5) if case != "no_rows" else (0, 5, 16, 8, 5)
+    nb, page, Lc, Rc = 6, 16, (13 if case == "odd_widths" else 512), (3 if case == "odd_widths" else 64)
+    ntok = 0 if case == "no_tokens" else 40
+    nope = _bits(mi.normal(81, T * H * L), dtype).reshape(T, H, L)
+    rope = _bits(mi.normal(82, T * Hr * R), dtype).reshape(T, Hr, R)
+    kv = _bits(mi.normal(83, ntok * Lc), dtype).reshape(ntok, Lc)
+    kp = _bits(mi.normal(84, ntok * Rc), dtype).reshape(ntok, Rc)
+    slots = mi.permutation(85, nb * page)[:ntok].copy()
+    if ntok:
+        slots[4] = -1
+    E = Lc + Rc
+    fill = _bits(np.full(nb * page * E, 0.5, np.float32), dtype)
+    cache = to_dev(fill, dtype).view(nb, page, E)
+    out = poisoned((T, H, L + R), dtype)
+    mla.mla_concat_q_cache_write(out, to_dev(nope, dtype), to_dev(rope, dtype), cache, to_dev(kv, dtype),
+                                 to_dev(kp, dtype), torch.from_numpy(slots).cuda())
+    mla.mla_device_error()
+    u = np.uint16 if dtype == "bf16" else np.uint32
+    assert np.array_equal(to_host_bits(out).view(u), orc.concat_q(nope, rope).view(u))
+    want = orc.cache_write(fill, 0, nb, page, (page * E, E, 1), kv, kp, slots)
+    assert np.array_equal(to_host_bits(cache).reshape(-1).view(u), want.view(u))

@@ -261,6 +261,32 @@ def test_decode_v3_more_units_than_tiles(mla):
     check_close(to_f64(o0), want, "bf16", "v3 decode, default units")
 
 
+@pytest.mark.parametrize("R", [0, 64])
+def test_decode_64_heads_tensor_core(mla, R):
+    # 64 heads (the memra NoPE geometry with R = 0, or a 64-head slice of V3 with rope) take the
+    # tensor-core decode with half of its 128-row tile masked: ragged lengths across page and tile
+    # boundaries, an empty sequence, several split counts, against the oracle.
+    H, L, page = 64, 512, 64
+    E = L + R
+    lens = [1, 37, 64, 65, 200, 0, 1000, 129]
+    need = [(n + page - 1) // page for n in lens]
+    nb = sum(need) + 3
+    perm = mi.permutation(160 + R, nb)
+    table = np.full((len(lens), max(need) + 1), -5, np.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    cache = mi.encode(mi.draw("normal", 161 + R, nb * page * E, 0.5), "bf16").reshape(nb, page, E)
+    q = mi.encode(mi.draw("normal", 162 + R, len(lens) * H * E, 0.5), "bf16").reshape(len(lens), H, E)
+    scale = 1.0 / math.sqrt(256 if R == 0 else 192)
+    want, want_lse = oracle_decode(q, cache, table, lens, "bf16", L, R, scale)
+    for splits in (0, 1, 3):
+        o, lse = run_decode(mla, q, cache, table, lens, "bf16", L, R, scale, splits)
+        check_close(to_f64(o), want, "bf16", f"64-head decode R={R}, splits {splits}")
+        check_lse(lse, want_lse, "bf16")
+
+
 @pytest.mark.parametrize("page", [8, 16, 32, 128])
 def test_decode_v3_tensor_core_page_sizes(mla, page):
     # The tensor-core path takes pages of 8, 16 and 32 rows (several TMA boxes per 64-key tile,
