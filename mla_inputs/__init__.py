@@ -431,3 +431,81 @@ def nope_prefill(n_seq: int = 4, seq_len: int = 2048) -> PrefillWorkload:
     """NoPE causal prefill: 64 heads, P=256, R=0, V=256, L=512, n_seq x seq_len."""
     return prefill_workload(NOPE_64, "bf16", [seq_len] * n_seq, [seq_len] * n_seq, 64,
                             config_index=4, scale=1.0 / math.sqrt(256))
+
+
+# ---------------------------------------------------------------------------- ds_mla sparse decode
+
+SEED_DS_MLA = 99
+
+
+def ds_mla_entries(seed: int, n: int, unit_scales: bool = False) -> np.ndarray:
+    """[n, 656] uint8 cache entries with the ds_mla byte structure, drawn directly (no
+    conversion of values): 512 e4m3 codes with a random sign, an exponent field in
+    [1, 9] and a random mantissa (about one in 64 a zero code), four little-endian
+    float32 scales (1.0, or uniform in [1/128, 1/32)), and 64 little-endian bf16 rope
+    values drawn N(0, 1) * 0.1."""
+    m = n * 512
+    code = (randint(seed, m, 0, 1) << 7) | (randint(seed + 1, m, 1, 9) << 3) | randint(seed + 2, m, 0, 7)
+    code = np.where(randint(seed + 3, m, 0, 63) == 0, 0, code).astype(np.uint8).reshape(n, 512)
+    if unit_scales:
+        sc = np.ones((n, 4), np.float32)
+    else:
+        sc = (1.0 / 128 + unit01(seed + 4, n * 4) * (1.0 / 32 - 1.0 / 128)).astype(np.float32).reshape(n, 4)
+    rope = to_bf16_bits(normal(seed + 5, n * 64) * np.float32(0.1)).reshape(n, 64)
+    return np.concatenate([code, sc.astype("<f4").view(np.uint8).reshape(n, 16),
+                           rope.astype("<u2").view(np.uint8).reshape(n, 128)], axis=1)
+
+
+@dataclasses.dataclass
+class SparseDecodeWorkload:
+    """Sparse top-k decode over a ds_mla cache seen as one layer of a block-major
+    multi-layer buffer: ``storage`` is the whole uint8 buffer [num_blocks, n_layers,
+    page, 656] (other layers random bytes), the layer's view has byte strides
+    (n_layers * page * 656, 656, 1) at byte offset layer * page * 656."""
+    q_cat: np.ndarray        # bf16 bits [B, H, 576]
+    storage: np.ndarray      # uint8, flat
+    indices: np.ndarray      # int32 [B, topk], -1 = padding
+    num_blocks: int
+    page: int
+    n_layers: int
+    layer: int
+    scale: float
+
+    @property
+    def offset(self) -> int:
+        return self.layer * self.page * 656
+
+    @property
+    def strides(self) -> tuple[int, int, int]:
+        return (self.n_layers * self.page * 656, 656, 1)
+
+
+def sparse_decode_workload(batch: int = 2, heads: int = 128, topk: int = 128, num_blocks: int = 32,
+                           page: int = 64, n_layers: int = 3, layer: int = 1, pattern: str = "blocks",
+                           unit_scales: bool = True, config_index: int = 7) -> SparseDecodeWorkload:
+    """``pattern`` "blocks": query b takes the first topk slots of its own num_blocks // batch
+    consecutive blocks, padded with -1 (the pages' layout); "scattered": query b takes a
+    random count in [0, topk] of distinct slots drawn from the whole cache in random order,
+    with the -1 padding shuffled among them."""
+    off = 1000 * config_index
+    E = 656
+    layer_bytes = ds_mla_entries(SEED_DS_MLA + off, num_blocks * page, unit_scales).reshape(num_blocks, page, E)
+    other = randint(SEED_DS_MLA + off + 10, num_blocks * n_layers * page * E, 0, 255).astype(np.uint8)
+    storage = other.reshape(num_blocks, n_layers, page, E)
+    storage[:, layer] = layer_bytes
+    idx = np.full((batch, topk), -1, np.int32)
+    if pattern == "blocks":
+        per = num_blocks // batch
+        for b in range(batch):
+            slots = np.arange(b * per * page, (b + 1) * per * page)[:topk]
+            idx[b, :slots.size] = slots
+    elif pattern == "scattered":
+        counts = randint(SEED_DS_MLA + off + 20, batch, 0, topk)
+        for b in range(batch):
+            slots = permutation(SEED_DS_MLA + off + 30 + b, num_blocks * page)[: int(counts[b])]
+            row = np.concatenate([slots, np.full(topk - slots.size, -1)])
+            idx[b] = row[permutation(SEED_DS_MLA + off + 30 + batch + b, topk)]
+    else:
+        raise ValueError(pattern)
+    q = to_bf16_bits(normal(SEED_Q_NOPE + off, batch * heads * 576) * np.float32(0.1)).reshape(batch, heads, 576)
+    return SparseDecodeWorkload(q, storage.reshape(-1), idx, num_blocks, page, n_layers, layer, 576 ** -0.5)

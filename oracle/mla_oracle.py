@@ -35,7 +35,13 @@ Readings where the pages are silent (each is listed in the design notes):
     to even, saturating finite values at +-448 (P3 passes a scale to the cache
     write and descale_q / descale_k to the fp8 decode but prints neither the
     conversion nor the dequantisation); reading one multiplies the code's value
-    by descale_k, and the query by descale_q.
+    by descale_k, and the query by descale_q;
+  * a ds_mla entry's four float32 scales each cover 128 consecutive latent
+    columns (scale g for columns 128g..128g+127), multiplied into the code's
+    value; the scales and the bf16 rope values are little-endian (P3 builds the
+    entry from tensors' bytes and says only "512B fp8 + 16B f32 scales + 128B
+    bf16 rope"); a sparse query attends each listed slot once per listing and
+    skips negative entries.
 """
 from __future__ import annotations
 
@@ -313,6 +319,64 @@ def decode_fp8(q_cat: np.ndarray, storage: np.ndarray, offset: int, page: int,
     values = e4m3_value(storage) * float(descale_k)
     return decode(np.asarray(q_cat) * float(descale_q), values, offset, page, strides, L, R,
                   block_table, seq_lens, scale, batch_ids)
+
+
+# ---------------------------------------------------------------------------
+# fp8 ds_mla sparse decode (P3, ``flash_mla_with_kvcache`` with
+# ``is_fp8_kvcache`` and ``indices``: a 656-byte entry per token, 512 bytes of
+# e4m3 latent codes, four float32 scales, 64 bf16 rope values; top-k int32
+# slot indices per query, -1 for padding)
+# ---------------------------------------------------------------------------
+
+DS_MLA_ENTRY = 656          # bytes of one cache entry
+DS_MLA_L = 512              # latent columns, stored as e4m3 codes in bytes 0..511
+DS_MLA_GROUP = 128          # latent columns per float32 scale (four scales, bytes 512..527)
+DS_MLA_R = 64               # rope columns, bf16 in bytes 528..655
+
+
+def ds_mla_values(entries: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """The values of [N, 656] ds_mla entries (uint8): c_kv [N, 512] and k_pe [N, 64],
+    float64. c_kv[n, i] = value(code[n, i]) * scale[n, i // 128], the scales read as
+    little-endian float32 from bytes 512..527; k_pe the little-endian bf16 values of
+    bytes 528..655."""
+    e = np.ascontiguousarray(entries, dtype=np.uint8).reshape(-1, DS_MLA_ENTRY)
+    n_groups = DS_MLA_L // DS_MLA_GROUP
+    scales = e[:, DS_MLA_L:DS_MLA_L + 4 * n_groups].copy().view("<f4").astype(np.float64)
+    rope_bits = e[:, DS_MLA_L + 4 * n_groups:].copy().view("<u2").astype(np.uint32)
+    k_pe = (rope_bits << 16).astype("<u4").view("<f4").astype(np.float64)
+    c_kv = e4m3_value(e[:, :DS_MLA_L]) * np.repeat(scales, DS_MLA_GROUP, axis=1)
+    return c_kv, k_pe
+
+
+def decode_sparse_ds_mla(q_cat: np.ndarray, storage: np.ndarray, offset: int, num_blocks: int,
+                         page: int, strides: Sequence[int], indices: np.ndarray, scale: float,
+                         batch_ids: Optional[Sequence[int]] = None) -> tuple[np.ndarray, np.ndarray]:
+    """Sparse decode over an fp8 ds_mla cache.
+
+    The cache is the flat byte ``storage`` seen as [num_blocks, page, 656] at byte
+    ``offset`` with byte ``strides``. Query b (q_cat [B, H, 576], float64) attends
+    the rows at slots indices[b, j] >= 0, slot = block * page + row, in any order,
+    each listed slot once per listing; negative entries are padding. The row's key
+    is [c_kv | k_pe] and its value c_kv (``ds_mla_values``); then it is
+    ``attend_absorbed``. A slot past the cache raises. Returns o_lat [n, H, 512]
+    and lse [n, H] for ``batch_ids`` (default: all); no valid slot gives (0, -inf).
+    """
+    s0, s1, s2 = strides
+    ids = range(q_cat.shape[0]) if batch_ids is None else batch_ids
+    storage = np.asarray(storage)
+    os_, ls_ = [], []
+    for b in ids:
+        sl = np.asarray(indices[b], dtype=np.int64)
+        sl = sl[sl >= 0]
+        if np.any(sl >= num_blocks * page):
+            raise ValueError(f"slot {int(sl.max())} past a cache of {num_blocks * page} rows")
+        base = offset + (sl // page) * s0 + (sl % page) * s1
+        ent = storage[base[:, None] + np.arange(DS_MLA_ENTRY, dtype=np.int64)[None, :] * s2]
+        c_kv, kp = ds_mla_values(ent)
+        o, lse = attend_absorbed(q_cat[b, :, :DS_MLA_L], q_cat[b, :, DS_MLA_L:], c_kv, kp, scale)
+        os_.append(o)
+        ls_.append(lse)
+    return np.stack(os_), np.stack(ls_)
 
 
 def prefill(q_cat: np.ndarray, cu_seqlens_q: np.ndarray, kv_lens: np.ndarray,

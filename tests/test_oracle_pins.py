@@ -589,3 +589,143 @@ def test_fp8_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_fp8_decode_equals_decode_on_the_same_values()
     monkeypatch.setattr(orc, "decode_fp8", good_dec)
+
+
+# ---------------------------------------------------------------------------- fp8 ds_mla sparse decode
+
+def _ds_mla_values_by_library(entries):
+    """The entries' values by other routes: torch's e4m3 and bf16 decoders, numpy's
+    little-endian float32 reader, and an explicit loop over the four 128-column groups."""
+    import torch
+    e = np.ascontiguousarray(entries, dtype=np.uint8).reshape(-1, 656)
+    n = e.shape[0]
+    codes = torch.from_numpy(e[:, :512].copy()).view(torch.float8_e4m3fn).double().numpy()
+    scales = np.frombuffer(e[:, 512:528].tobytes(), dtype="<f4").reshape(n, 4).astype(np.float64)
+    rope = torch.from_numpy(e[:, 528:].copy()).view(torch.bfloat16).double().numpy()
+    c_kv = codes.copy()
+    for g in range(4):
+        c_kv[:, 128 * g:128 * (g + 1)] *= scales[:, g:g + 1]
+    return c_kv, rope
+
+
+def test_ds_mla_entry_values_follow_the_byte_layout():
+    ent = mi.ds_mla_entries(8101, 40)
+    c_kv, k_pe = orc.ds_mla_values(ent)
+    want_c, want_r = _ds_mla_values_by_library(ent)
+    assert c_kv.shape == (40, 512) and k_pe.shape == (40, 64)
+    assert np.array_equal(c_kv, want_c) and np.array_equal(k_pe, want_r)
+    # a hand-built entry: code 0x38 (1.0) in column 130 (group 1, scale 0.25), code 0xC0
+    # (-2.0) in column 511 (group 3, scale 3.0), rope column 5 = bf16 0x4040 (3.0)
+    e = np.zeros((1, 656), np.uint8)
+    e[0, 130], e[0, 511] = 0x38, 0xC0
+    e[0, 512:528] = np.array([1.0, 0.25, 1.0, 3.0], "<f4").view(np.uint8)
+    e[0, 528 + 10], e[0, 528 + 11] = 0x40, 0x40
+    c, r = orc.ds_mla_values(e)
+    assert c[0, 130] == 0.25 and c[0, 511] == -6.0 and np.count_nonzero(c) == 2
+    assert r[0, 5] == 3.0 and np.count_nonzero(r) == 1
+
+
+def _sparse_small(pattern, unit_scales, batch=3, heads=4, topk=96, num_blocks=12, page=16, seed_cfg=7):
+    w = mi.sparse_decode_workload(batch=batch, heads=heads, topk=topk, num_blocks=num_blocks, page=page,
+                                  pattern=pattern, unit_scales=unit_scales, config_index=seed_cfg)
+    q = mi.decode_f64(w.q_cat, "bf16")
+    return w, q
+
+
+@pytest.mark.parametrize("pattern,unit_scales", [("blocks", True), ("scattered", False)])
+def test_sparse_decode_equals_paged_decode_of_the_listed_rows(pattern, unit_scales):
+    # page-1 paged decode whose block table is the list of valid slots, over float64 values of
+    # the contiguous layer decoded by the library routes
+    w, q = _sparse_small(pattern, unit_scales)
+    layer = w.storage.reshape(w.num_blocks, w.n_layers, w.page, 656)[:, w.layer].reshape(-1, 656)
+    c_kv, k_pe = _ds_mla_values_by_library(layer)
+    values = np.concatenate([c_kv, k_pe], axis=1).reshape(-1)
+    valid = [w.indices[b][w.indices[b] >= 0].astype(np.int64) for b in range(q.shape[0])]
+    table = np.zeros((q.shape[0], max(1, max(v.size for v in valid))), np.int64)
+    for b, v in enumerate(valid):
+        table[b, :v.size] = v
+    lens = np.array([v.size for v in valid])
+    o_d, l_d = orc.decode(q, values, 0, 1, (576, 576, 1), 512, 64, table, lens, w.scale)
+    o_s, l_s = orc.decode_sparse_ds_mla(q, w.storage, w.offset, w.num_blocks, w.page, w.strides,
+                                        w.indices, w.scale)
+    assert np.array_equal(o_s, o_d) and np.array_equal(l_s, l_d)
+    assert np.isfinite(o_s).all() or (lens == 0).any()
+
+
+def test_sparse_decode_is_order_free_and_skips_padding():
+    w, q = _sparse_small("scattered", False, batch=4)
+    o0, l0 = orc.decode_sparse_ds_mla(q, w.storage, w.offset, w.num_blocks, w.page, w.strides, w.indices, w.scale)
+    idx = w.indices[:, ::-1].copy()                                   # reversed
+    idx = np.concatenate([np.full((idx.shape[0], 7), -1, np.int32), idx], axis=1)   # more padding
+    o1, l1 = orc.decode_sparse_ds_mla(q, w.storage, w.offset, w.num_blocks, w.page, w.strides, idx, w.scale)
+    assert np.allclose(o1, o0, rtol=1e-12, atol=1e-14) and np.allclose(l1, l0, rtol=1e-13)
+
+
+def test_sparse_decode_duplicate_listing_doubles_the_weight():
+    w, q = _sparse_small("blocks", False, batch=1, heads=3)
+    a, b = 5, 17
+    o, lse = orc.decode_sparse_ds_mla(q, w.storage, w.offset, w.num_blocks, w.page, w.strides,
+                                      np.array([[a, -1, b, a]]), w.scale)
+    layer = w.storage.reshape(w.num_blocks, w.n_layers, w.page, 656)[:, w.layer].reshape(-1, 656)
+    c_kv, k_pe = _ds_mla_values_by_library(layer[[a, b]])
+    k = np.concatenate([c_kv, k_pe], axis=1)
+    s = w.scale * (q[0] @ k.T)                                        # [H, 2]
+    wa, wb = 2 * np.exp(s[:, 0]), np.exp(s[:, 1])
+    want = (wa[:, None] * c_kv[0] + wb[:, None] * c_kv[1]) / (wa + wb)[:, None]
+    assert np.allclose(o[0], want, rtol=1e-12, atol=1e-15)
+    assert np.allclose(lse[0], np.log(wa + wb), rtol=1e-13)
+
+
+def test_sparse_decode_empty_single_and_out_of_range():
+    w, q = _sparse_small("blocks", False, batch=2, heads=3)
+    idx = np.array([[-1, -1, -1], [-1, 40, -1]])
+    o, lse = orc.decode_sparse_ds_mla(q, w.storage, w.offset, w.num_blocks, w.page, w.strides, idx, w.scale)
+    assert np.array_equal(o[0], np.zeros((3, 512))) and np.all(lse[0] == -np.inf)
+    layer = w.storage.reshape(w.num_blocks, w.n_layers, w.page, 656)[:, w.layer].reshape(-1, 656)
+    c_kv, k_pe = _ds_mla_values_by_library(layer[[40]])
+    assert np.allclose(o[1], np.broadcast_to(c_kv[0], (3, 512)), rtol=1e-14, atol=0)
+    s = w.scale * (q[1] @ np.concatenate([c_kv[0], k_pe[0]]))
+    assert np.allclose(lse[1], s, rtol=1e-13)
+    with pytest.raises(ValueError):
+        orc.decode_sparse_ds_mla(q, w.storage, w.offset, w.num_blocks, w.page, w.strides,
+                                 np.array([[0, w.num_blocks * w.page], [1, 2]]), w.scale)
+
+
+def test_sparse_planted_mistakes_are_caught(monkeypatch):
+    good_values = orc.ds_mla_values
+
+    def groups_reversed(entries):
+        e = np.ascontiguousarray(entries, dtype=np.uint8).reshape(-1, 656).copy()
+        sc = e[:, 512:528].reshape(-1, 4, 4)[:, ::-1].reshape(-1, 16)
+        e[:, 512:528] = sc
+        return good_values(e)
+
+    def rope_big_endian(entries):
+        e = np.ascontiguousarray(entries, dtype=np.uint8).reshape(-1, 656).copy()
+        e[:, 528:] = e[:, 528:].reshape(-1, 64, 2)[:, :, ::-1].reshape(-1, 128)
+        return good_values(e)
+
+    for bad in (groups_reversed, rope_big_endian):
+        monkeypatch.setattr(orc, "ds_mla_values", bad)
+        with pytest.raises(AssertionError), np.errstate(invalid="ignore"):   # swapped bytes make NaNs
+            test_ds_mla_entry_values_follow_the_byte_layout()
+    monkeypatch.setattr(orc, "ds_mla_values", good_values)
+    good_dec = orc.decode_sparse_ds_mla
+
+    def padding_as_slot_zero(q, st, off, nb, page, strides, idx, scale, batch_ids=None):
+        return good_dec(q, st, off, nb, page, strides, np.maximum(idx, 0), scale, batch_ids)
+
+    def row_and_block_swapped(q, st, off, nb, page, strides, idx, scale, batch_ids=None):
+        idx = np.asarray(idx)
+        sw = np.where(idx >= 0, (idx % page) * page + idx // page, idx) if nb == page else idx
+        s0, s1, s2 = strides
+        return good_dec(q, st, off, nb, page, (s1, s0, s2), idx, scale, batch_ids) if nb != page else \
+            good_dec(q, st, off, nb, page, strides, sw, scale, batch_ids)
+
+    monkeypatch.setattr(orc, "decode_sparse_ds_mla", padding_as_slot_zero)
+    with pytest.raises(AssertionError):
+        test_sparse_decode_is_order_free_and_skips_padding()
+    monkeypatch.setattr(orc, "decode_sparse_ds_mla", row_and_block_swapped)
+    with pytest.raises((AssertionError, IndexError)):
+        test_sparse_decode_equals_paged_decode_of_the_listed_rows("scattered", False)
+    monkeypatch.setattr(orc, "decode_sparse_ds_mla", good_dec)
