@@ -3,8 +3,9 @@
 A step is one decode step of the large V3 workload: 64 sequences, 128 heads,
 context lengths drawn uniformly from [1024, 16384], page 64, random block
 table; bf16 storage, fp32 accumulation. One step runs every stage of the path
-through the C ABI: absorb (W_UK fold) -> q concat -> cache write of the new
-rows -> split-KV decode (schedule, split kernel, LSE combine) -> v_up (W_UV).
+through the C ABI: absorb (W_UK fold) -> q concat and cache write of the new
+rows (one launch) -> split-KV decode (schedule, split kernel, LSE combine) ->
+v_up (W_UV).
 Inputs are resident in HBM before the timed region; the latent cache (about
 0.56 GB) is larger than L2 (129 MB), so no flush is needed between steps.
 
@@ -53,17 +54,34 @@ def _peaks() -> dict:
                 bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def decode_algorithmic_bytes(seq_lens, B, H, L, R, max_blocks, es=2) -> int:
-    """Bytes the decode stage must move: every cached row once, q_cat in, o_lat out,
-    the block-table entries in use and the lengths."""
+def decode_algorithmic_bytes(seq_lens, B, H, L, R, max_blocks, es=2, cache_es=None) -> int:
+    """Bytes the decode stage must move: every cached row once (cache_es bytes an element,
+    1 for an e4m3 cache), q_cat in, o_lat out, the block-table entries in use and the lengths."""
     E = L + R
+    ce = es if cache_es is None else cache_es
     rows = int(sum(int(n) for n in seq_lens))
     pages = int(sum((int(n) + 63) // 64 for n in seq_lens))
-    return rows * E * es + B * H * E * es + B * H * L * es + pages * 4 + B * 4
+    return rows * E * ce + B * H * E * es + B * H * L * es + pages * 4 + B * 4
 
 
 def decode_algorithmic_flops(seq_lens, H, L, R) -> int:
     return int(sum(int(n) for n in seq_lens)) * H * 2 * ((L + R) + L)
+
+
+def roofline(nbytes: float, flops: float, ms: float, peaks: dict, sustained: bool = False) -> dict:
+    """Roofline figures of one launch against the tighter of its two bounds: HBM bytes at the
+    measured copy rate, or bf16 tensor flops at the measured GEMM rate (burst for a kernel timed
+    alone, sustained for one timed inside a long step)."""
+    tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (tc_peak * 1e12)
+    sec = ms * 1e-3
+    if t_hbm >= t_tc:
+        r = {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    return r
 
 
 class ClockSampler:
@@ -147,7 +165,7 @@ def _traffic_for(kernel_src: str) -> float | None:
 # --------------------------------------------------------------------------- the workload
 
 class DecodeStep:
-    """Device-resident inputs of one decode step and the five calls that run it."""
+    """Device-resident inputs of one decode step and the four calls that run it."""
 
     def __init__(self, mla, w, device, rank_seed=0):
         import numpy as np
@@ -177,31 +195,22 @@ class DecodeStep:
         self.o_lat = torch.empty((B, H, L), dtype=dt, device=device)
         self.out = torch.empty((B, H, V), dtype=dt, device=device)
         self.ws = torch.empty(mla.mla_decode_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
-        self.launches_per_step = 7
-        # the cache write does not depend on the query path (absorb, concat): it runs on a side
-        # stream concurrently with it and joins before the decode
-        self.side = torch.cuda.Stream(device)
-        self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
+        # absorb (1) + concat and cache write (1) + decode (schedule, split, combine: 3) + v_up (1)
+        self.launches_per_step = 6
 
     def run(self, ev_decode=None, q_nope=None, q_pe=None, kv_c=None, k_pe=None, slots=None,
             table=None, lens=None, out=None):
-        import torch
         m = self.mla
         out = self.out if out is None else out
         q_nope = self.q_nope if q_nope is None else q_nope
-        main = torch.cuda.current_stream()
-        self.ev_fork.record(main)
-        self.side.wait_event(self.ev_fork)
-        with torch.cuda.stream(self.side):
-            m.mla_cache_write(self.cache, self.new_kv_c if kv_c is None else kv_c,
-                              self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
-            self.ev_join.record(self.side)
         # the absorb writes q_lat straight into q_cat's first L columns (a [H,B,L] view of it),
-        # so the concat finds its nope operand in place and copies only the rope columns
+        # so the concat finds its nope operand in place and moves only the rope columns, in the
+        # same launch as the cache write of the new rows
         lat = self.q_cat[:, :, :self.L]
         m.mla_absorb_q(lat.transpose(0, 1), q_nope.transpose(0, 1), self.w_uk)
-        m.mla_concat_q(self.q_cat, lat, self.q_pe if q_pe is None else q_pe)
-        main.wait_event(self.ev_join)
+        m.mla_concat_q_cache_write(self.q_cat, lat, self.q_pe if q_pe is None else q_pe, self.cache,
+                                   self.new_kv_c if kv_c is None else kv_c,
+                                   self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
         if ev_decode is not None:
             ev_decode[0].record()
         m.mla_decode(self.o_lat, self.q_cat, self.cache, self.table if table is None else table,
@@ -416,7 +425,7 @@ def run_ours(args) -> None:
     clocks = clk.summary()
 
     # end to end through the same calls with host buffers: every step copies its inputs in from
-    # pinned host memory, runs the five calls and copies its output back; like a serving loop,
+    # pinned host memory, runs the four calls and copies its output back; like a serving loop,
     # the copies of neighbouring steps run on two copy streams under the compute (two sets of
     # device buffers, ordered by events), and the timed region ends when the last output is back
     def pinned(t):
@@ -464,8 +473,11 @@ def run_ours(args) -> None:
                  slots=d["slots"], table=d["table"], lens=d["lens"], out=dev_out[b])
 
     # like a serving loop, the step goes to the GPU as one CUDA graph per input buffer set: the
-    # five calls (seven kernels, the cache write on a side branch) are captured once through the
+    # four calls (six kernels) are captured once through the
     # same C ABI and replayed, so the host's per-call marshalling is paid once, not every step
+    for b in range(2):                                 # the first eager runs read real inputs
+        dev_buf[b].copy_(host_buf)
+    torch.cuda.synchronize()
     graphs, launch = [], "cuda_graph"
     try:
         for b in range(2):
@@ -529,11 +541,8 @@ def run_ours(args) -> None:
     if rank != 0:
         return
     peaks = _peaks()
-    total_bytes = bytes_step * world
     value = job_throughput(bytes_step, ms_step, world)
-    achieved = bytes_step / (decode_ms * 1e-3) / 1e9
-    t_hbm = bytes_step / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flops_step / (peaks["bf16_tflops"] * 1e12)
+    rl = roofline(bytes_step, flops_step, decode_ms, peaks, sustained=True)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -543,15 +552,13 @@ def run_ours(args) -> None:
                    "rope_dim": R, "page": w.page, "context": "U[1024,16384] per sequence",
                    "cached_rows": int(w.seq_lens.sum()), "l2": "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
-        "roofline": {"kernel": "mla_decode (schedule + split + combine)", "bound":
-                     "hbm" if t_hbm >= t_tc else "tensor", "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"],
+        "roofline": {"kernel": "mla_decode (schedule + split + combine)", **rl,
                      "traffic": _traffic_for("attn_tc.cu") if os.path.exists(
                          os.path.join(ROOT, "mla_latent_kv_11_gb300", "csrc", "attn_tc.cu")) else None,
                      "peak_source": peaks["source"], "ms_per_launch": decode_ms,
                      "bytes_per_launch": bytes_step, "flops_per_launch": flops_step,
-                     "tensor_frac": flops_step / (decode_ms * 1e-3) / (peaks["bf16_tflops"] * 1e12)},
+                     "hbm_frac": bytes_step / (decode_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "tensor_frac": flops_step / (decode_ms * 1e-3) / (peaks["bf16_tflops_sustained"] * 1e12)},
         "e2e": {"value": job_throughput(bytes_step, e2e_ms, world), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "launch": launch},
         "gpu_launches": step.launches_per_step * args.steps,
@@ -562,14 +569,18 @@ def run_ours(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def component_figures(mla, mi, device) -> dict:
-    """Per-stage figures on the other workloads: prefill TFLOP/s, decode at a fixed 8192
-    context, concat and cache-write GB/s."""
+def component_figures(mla, mi, device, only=None) -> dict:
+    """Per-stage figures on the other workloads, each against the tighter of its rooflines:
+    NoPE prefill, decode at a fixed 8192 context (bf16 and e4m3 cache, 128 heads; bf16 at 64
+    heads), and the copy kernels. The copies run far shorter than a host call, so they are
+    timed as device time: many launches captured in one CUDA graph, replayed between events,
+    cycling through enough input sets to exceed L2."""
     import numpy as np
     import torch
     out = {}
     peaks = _peaks()
     torch.manual_seed(1234)
+    l2_bytes = 129 * 2 ** 20
 
     def timed(fn, reps=10, warm=3):
         for _ in range(warm):
@@ -583,10 +594,45 @@ def component_figures(mla, mi, device) -> dict:
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
+    def device_timed(fns, per_graph=64, reps=5):
+        """Mean device time of one call: per_graph calls (cycling through fns) in one graph."""
+        for f in fns:
+            f()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(per_graph):
+                fns[i % len(fns)]()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * per_graph)
+
     def dev(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(device).view(torch.bfloat16)
 
-    # NoPE causal prefill, 64 heads, 4 x 2048
+    def want(group):
+        return only is None or group in only
+
+    if want("prefill"):
+        prefill_figures(mla, mi, device, out, peaks, timed)
+    if want("decode"):
+        decode_figures(mla, mi, device, out, peaks, timed)
+    if want("copy"):
+        copy_figures(mla, mi, device, out, peaks, dev, device_timed, l2_bytes)
+    return out
+
+
+def prefill_figures(mla, mi, device, out, peaks, timed) -> None:
+    """NoPE causal prefill, 64 heads, 4 x 2048."""
+    import numpy as np
+    import torch
     H, L, page, n_seq, S = 64, 512, 64, 4, 2048
     T = n_seq * S
     q = torch.randn((T, H, L), device=device, dtype=torch.bfloat16) * 0.7
@@ -598,45 +644,104 @@ def component_figures(mla, mi, device) -> dict:
     o = torch.empty((T, H, L), dtype=torch.bfloat16, device=device)
     ms = timed(lambda: mla.mla_prefill(o, q, cache, table, cu, kv, S, L, 0, 1.0 / 16.0), reps=3, warm=1)
     flops = n_seq * (S * (S + 1) // 2) * H * 2 * (L + L)
+    nbytes = (2 * T * H * L + T * L) * 2
     out["prefill_nope_h64_4x2048"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
-                                      "frac_of_bf16_peak": flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12)}
+                                      "frac_of_bf16_peak": flops / (ms * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+                                      "roofline": roofline(nbytes, flops, ms, peaks)}
     del q, cache, o
-    # decode at a fixed 8192-token context: 64 sequences, 128 heads, page 64, a seeded block
-    # permutation (the "batch 64 x 8K context" reading of the large decode)
-    B, H, L, R, page, ctx = 64, 128, 512, 64, 64, 8192
-    E, nbl = L + R, ctx // page
-    cache = torch.randn((B * nbl, page, E), device=device, dtype=torch.bfloat16) * 0.1
+
+
+def decode_figures(mla, mi, device, out, peaks, timed) -> None:
+    """Decode at a fixed 8192-token context: 64 sequences, page 64, a seeded block permutation
+    (the "batch 64 x 8K context" reading of the large decode); 128 heads with a 64-wide rope
+    part (bf16 and e4m3 cache), and the 64-head NoPE geometry (no rope part)."""
+    import numpy as np
+    import torch
+    B, L, page, ctx = 64, 512, 64, 8192
+    nbl = ctx // page
     table = torch.from_numpy(mi.permutation(8192, B * nbl).astype(np.int32).reshape(B, nbl)).to(device)
     lens = torch.full((B,), ctx, dtype=torch.int32, device=device)
-    q = torch.randn((B, H, E), device=device, dtype=torch.bfloat16) * 0.1
-    o = torch.empty((B, H, L), dtype=torch.bfloat16, device=device)
-    ws = torch.empty(mla.mla_decode_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
-    ms = timed(lambda: mla.mla_decode(o, q, cache, table, lens, L, R, 1.0 / math.sqrt(192), workspace=ws), reps=20)
-    nbytes = decode_algorithmic_bytes([ctx] * B, B, H, L, R, nbl)
-    out["decode_b64_ctx8192_fixed"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
-                                       "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                                       "queries_per_s": B / (ms * 1e-3)}
-    del cache, table, q, o, ws
-    # concat and cache write, unified-slot workload
+    for H, R, name in ((128, 64, "decode_b64_ctx8192_fixed"), (64, 0, "decode_h64_nope_b64_ctx8192_fixed")):
+        E = L + R
+        cache = torch.randn((B * nbl, page, E), device=device, dtype=torch.bfloat16) * 0.1
+        q = torch.randn((B, H, E), device=device, dtype=torch.bfloat16) * 0.1
+        o = torch.empty((B, H, L), dtype=torch.bfloat16, device=device)
+        ws = torch.empty(mla.mla_decode_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
+        ms = timed(lambda: mla.mla_decode(o, q, cache, table, lens, L, R, 1.0 / math.sqrt(192), workspace=ws),
+                   reps=20)
+        nbytes = decode_algorithmic_bytes([ctx] * B, B, H, L, R, nbl)
+        flops = decode_algorithmic_flops([ctx] * B, H, L, R)
+        out[name] = {"ms": ms, "heads": H, "rope_dim": R, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "queries_per_s": B / (ms * 1e-3), "roofline": roofline(nbytes, flops, ms, peaks)}
+        if H == 128:
+            # the same rows in an e4m3 cache (scale 1/16), 576-byte rows
+            scale = torch.full((1,), 1.0 / 16.0, dtype=torch.float32, device=device)
+            rows = cache.view(-1, E)
+            cache8 = torch.empty((B * nbl, page, E), dtype=torch.uint8, device=device)
+            slots = torch.arange(rows.shape[0], dtype=torch.int64, device=device)
+            mla.mla_cache_write_fp8(cache8, rows[:, :L], rows[:, L:], slots, scale)
+            ms8 = timed(lambda: mla.mla_decode_fp8(o, q, cache8, table, lens, L, R, 1.0 / math.sqrt(192),
+                                                   descale_k=scale, workspace=ws), reps=3, warm=1)
+            nbytes8 = decode_algorithmic_bytes([ctx] * B, B, H, L, R, nbl, cache_es=1)
+            out["decode_fp8_b64_ctx8192_fixed"] = {
+                "ms": ms8, "gbs": nbytes8 / (ms8 * 1e-3) / 1e9, "queries_per_s": B / (ms8 * 1e-3),
+                "path": "CUDA-core split kernel (e4m3 rows converted on load)",
+                "roofline": roofline(nbytes8, flops, ms8, peaks)}
+            del cache8, rows, slots
+        del cache, q, o, ws
+    del table, lens
+
+
+def copy_figures(mla, mi, device, out, peaks, dev, device_timed, l2_bytes) -> None:
+    """Concat and cache write, unified-slot workload (64 tokens x 128 heads; 200 new rows into
+    the middle layer of a 3-layer cache); the concat inputs come in enough copies to exceed L2."""
+    import torch
     w = mi.write_concat_workload()
     Nh, Bq, Lq = w.q_nope_storage.shape
-    store = dev(w.q_nope_storage)
-    nope = store.as_strided((Bq, Nh, Lq), (Lq, Bq * Lq, 1))
-    rope = dev(w.q_pe)
-    qc = torch.empty((Bq, Nh, Lq + w.q_pe.shape[2]), dtype=torch.bfloat16, device=device)
-    ms = timed(lambda: mla.mla_concat_q(qc, nope, rope), reps=50)
-    nbytes = 2 * qc.numel() * 2
-    out["concat_q_64x128"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    Rq = w.q_pe.shape[2]
+    q_bytes = 2 * Bq * Nh * (Lq + Rq) * 2
+    n_sets = max(2, -(-2 * l2_bytes // q_bytes))
+    sets = []
+    for _ in range(n_sets):
+        store = dev(w.q_nope_storage)
+        sets.append((store.as_strided((Bq, Nh, Lq), (Lq, Bq * Lq, 1)), dev(w.q_pe),
+                     torch.empty((Bq, Nh, Lq + Rq), dtype=torch.bfloat16, device=device)))
+    ms = device_timed([lambda s=s: mla.mla_concat_q(s[2], s[0], s[1]) for s in sets])
+    out["concat_q_64x128"] = {"ms": ms, "gbs": q_bytes / (ms * 1e-3) / 1e9,
+                              "roofline": roofline(q_bytes, 0, ms, peaks), "timing": f"device ({n_sets} input sets)"}
     E = w.entry
     big = torch.zeros((w.num_blocks, w.n_layers * w.page * E), dtype=torch.bfloat16, device=device)
     view = big.view(-1).as_strided((w.num_blocks, w.page, E), (w.n_layers * w.page * E, E, 1),
                                    w.layer * w.page * E)
     kv_c, k_pe = dev(w.kv_c), dev(w.k_pe)
     slots = torch.from_numpy(w.slots).to(device)
-    ms = timed(lambda: mla.mla_cache_write(view, kv_c, k_pe, slots), reps=50)
-    nbytes = 2 * w.kv_c.shape[0] * E * 2 + w.slots.size * 8
-    out["cache_write_200tok_unified_view"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9}
-    return out
+    ms = device_timed([lambda: mla.mla_cache_write(view, kv_c, k_pe, slots)])
+    c_bytes = 2 * w.kv_c.shape[0] * E * 2 + w.slots.size * 8
+    out["cache_write_200tok_unified_view"] = {"ms": ms, "gbs": c_bytes / (ms * 1e-3) / 1e9,
+                                              "timing": "device (200 rows: launch-latency bound)"}
+    # both in one launch, the step's form: rope columns into q_cat after an in-place absorb
+    fused = []
+    for s in sets:
+        q_cat = s[2]
+        fused.append(lambda q_cat=q_cat, r=s[1]: mla.mla_concat_q_cache_write(
+            q_cat, q_cat[:, :, :Lq], r, view, kv_c, k_pe, slots))
+    ms = device_timed(fused)
+    f_bytes = 2 * Bq * Nh * Rq * 2 + c_bytes
+    out["concat_rope_and_cache_write_one_launch"] = {"ms": ms, "gbs": f_bytes / (ms * 1e-3) / 1e9,
+                                                     "timing": f"device ({n_sets} input sets)"}
+
+
+def run_components(only) -> None:
+    """The chosen per-stage figures alone on this process's GPU (for profiling one kernel)."""
+    import torch
+    import mla_latent_kv_11_gb300 as mla
+    from mla_latent_kv_11_gb300 import build as mla_build
+    import mla_inputs as mi
+    mla_build.build()
+    mla.lib()
+    torch.cuda.set_device(0)
+    print(json.dumps({"components": component_figures(mla, mi, "cuda:0", only=set(only))}), flush=True)
 
 
 def main() -> None:
@@ -647,11 +752,15 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-components", action="store_true", help="skip the per-stage figures")
+    ap.add_argument("--component", action="append", choices=["prefill", "decode", "copy"],
+                    help="run only these per-stage figures (no decode step) and print them")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.component:
+        run_components(args.component)
     else:
         run_ours(args)
 

@@ -28,6 +28,32 @@ def test_decode_flops_are_qk_over_the_entry_and_pv_over_the_latent():
     assert bench.decode_algorithmic_flops([3, 5], H=2, L=4, R=2) == 8 * 2 * 2 * (6 + 4)
 
 
+def test_fp8_cache_rows_count_one_byte_an_element():
+    lens, B, H, L, R = [64, 65], 2, 2, 4, 2
+    bf16 = bench.decode_algorithmic_bytes(lens, B, H, L, R, 2)
+    fp8 = bench.decode_algorithmic_bytes(lens, B, H, L, R, 2, cache_es=1)
+    assert bf16 - fp8 == (64 + 65) * (L + R)
+
+
+def test_roofline_follows_the_tighter_bound():
+    peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0, "bf16_tflops_sustained": 50.0}
+    # 1 GB at 1000 GB/s = 1 ms; 10 GFLOP at 100 TFLOP/s = 0.1 ms: HBM is tighter
+    r = bench.roofline(1e9, 1e10, 2.0, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(500.0) and r["frac"] == pytest.approx(0.5)
+    # 1 GB (1 ms) against 200 GFLOP (2 ms at burst, 4 ms sustained): tensor is tighter
+    r = bench.roofline(1e9, 2e11, 8.0, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 100.0
+    assert r["frac"] == pytest.approx(0.25)
+    r = bench.roofline(1e9, 2e11, 8.0, peaks, sustained=True)
+    assert r["peak"] == 50.0 and r["frac"] == pytest.approx(0.5)
+    # frac is the bound's time over the measured time either way
+    for nbytes, flops, ms in ((3e9, 1e10, 7.0), (1e8, 5e11, 9.0)):
+        r = bench.roofline(nbytes, flops, ms, peaks)
+        t_bound = max(nbytes / 1e12, flops / 1e14) * 1e3
+        assert r["frac"] == pytest.approx(t_bound / ms)
+
+
 def test_job_throughput_is_all_ranks_bytes_over_the_slowest_step():
     assert bench.job_throughput(1e9, 1.0, 1) == pytest.approx(1000.0)
     assert bench.job_throughput(1e9, 2.0, 4) == pytest.approx(2000.0)
