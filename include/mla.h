@@ -200,6 +200,31 @@ mla_status mla_decode_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out,
                           const float* descale_k, int32_t num_splits, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* Bytes of one fp8 ds_mla cache entry: 512 e4m3 latent codes, four float32
+ * scales (scale g covers latent columns 128g .. 128g+127), 64 bf16 rope values. */
+#define MLA_DS_MLA_ENTRY_BYTES 656
+
+/* Step 4, sparse fp8 - top-k decode over an fp8 ds_mla cache ([vllm]
+ * flash_mla_with_kvcache with is_fp8_kvcache and indices, the DeepSeek sparse
+ * attention path; the indexer that picks the slots is not part of this library).
+ *   o_lat_out [B,H,512] (written), lse_out device float [B,H] or NULL,
+ *   q_cat [B,H,576] (latent 512 | rope 64), both in `dtype`;
+ *   cache [num_blocks, page, 656] byte view (strides in bytes, any stride(0) and
+ *   storage offset: one layer of a unified-slot buffer), data and strides 16-byte
+ *   aligned; indices: device int32 [B, topk] with row stride indices_stride
+ *   (>= topk); slot = block * page + row; negative entries are padding.
+ *   Query b attends the rows at its listed slots (each once per listing, in any
+ *   order): key [c_kv | k_pe], value c_kv, c_kv[i] = e4m3 value * scale[i / 128]
+ *   and k_pe the bf16 rope values; the softmax and outputs as mla_decode. A query
+ *   with no valid slot gets o = 0, lse = -inf. A slot past the cache is skipped and
+ *   reported by mla_device_error (MLA_ERR_DEVICE_DATA).
+ *   num_splits, workspace: as mla_decode, sized by
+ *   mla_decode_workspace_size(B, H, 512, num_splits). */
+mla_status mla_decode_sparse_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                                 mla_tensor cache, const int32_t* indices, int64_t indices_stride,
+                                 int32_t topk, float softmax_scale, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Step 4, prefill - causal attention of many queries per sequence over the same
  * paged cache ([memra] gate 1: pure prefill t_q == t_kv and the chunked shape
  * where the queries are a suffix of an already populated cache).

@@ -500,11 +500,14 @@ def sparse_decode_workload(batch: int = 2, heads: int = 128, topk: int = 128, nu
             slots = np.arange(b * per * page, (b + 1) * per * page)[:topk]
             idx[b, :slots.size] = slots
     elif pattern == "scattered":
-        counts = randint(SEED_DS_MLA + off + 20, batch, 0, topk)
+        n = num_blocks * page
+        counts = np.minimum(randint(SEED_DS_MLA + off + 20, batch, 0, topk), n)
+        starts = randint(SEED_DS_MLA + off + 21, batch, 0, n - 1)
+        perm = permutation(SEED_DS_MLA + off + 22, n)
         for b in range(batch):
-            slots = permutation(SEED_DS_MLA + off + 30 + b, num_blocks * page)[: int(counts[b])]
+            slots = perm[(int(starts[b]) + np.arange(int(counts[b]))) % n]    # distinct, scattered
             row = np.concatenate([slots, np.full(topk - slots.size, -1)])
-            idx[b] = row[permutation(SEED_DS_MLA + off + 30 + batch + b, topk)]
+            idx[b] = row[permutation(SEED_DS_MLA + off + 30 + b, topk)]
     else:
         raise ValueError(pattern)
     q = to_bf16_bits(normal(SEED_Q_NOPE + off, batch * heads * 576) * np.float32(0.1)).reshape(batch, heads, 576)

@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "mla_concat_q_cache_write": ([ctypes.c_int, T, T, T, T, T, T, P, I64, P], ctypes.c_int),
             "mla_decode_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, P, P, I32, P, SZ, P],
                                ctypes.c_int),
+            "mla_decode_sparse_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, F32, I32, P, SZ, P], ctypes.c_int),
             "mla_device_error": ([P], ctypes.c_int),
             "mla_check_bounded_wait": ([ctypes.c_uint32, P], ctypes.c_int),
         }
@@ -255,6 +256,33 @@ def mla_decode_fp8(o_lat_out, q_cat, cache, block_table, seq_lens, kv_lora_rank:
                                 _f32_scalar(descale_q, "descale_q"), _f32_scalar(descale_k, "descale_k"),
                                 num_splits, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                 _stream(stream)))
+
+
+def mla_decode_sparse_fp8(o_lat_out, q_cat, cache, indices, softmax_scale: float, lse_out=None,
+                          num_splits: int = 0, workspace=None, stream=None) -> None:
+    """Sparse top-k decode over an fp8 ds_mla cache: query b attends the slots indices[b]
+    (int32 [B, topk] or [B, 1, topk], -1 = padding) of a uint8 [num_blocks, page, 656]
+    (or [num_blocks, page, 1, 656]) cache; o_lat_out [B,H,512], q_cat [B,H,576]."""
+    import torch
+    if cache.dtype != torch.uint8:
+        raise MlaError(MLA_ERR_INVALID_ARG, "a ds_mla cache is uint8 bytes")
+    if cache.dim() == 4 and cache.shape[2] == 1:
+        cache = cache[:, :, 0]
+    if indices.dim() == 3 and indices.shape[1] == 1:
+        indices = indices[:, 0]
+    if indices.dtype != torch.int32 or indices.dim() != 2 or (indices.numel() and indices.stride(1) != 1):
+        raise MlaError(MLA_ERR_INVALID_ARG, "indices must be int32 [B, topk] with unit column stride")
+    if lse_out is not None and (lse_out.dtype != torch.float32 or not lse_out.is_contiguous()):
+        raise MlaError(MLA_ERR_INVALID_ARG, "lse_out must be contiguous float32")
+    B, H = q_cat.shape[0], q_cat.shape[1]
+    if workspace is None:
+        workspace = torch.empty(mla_decode_workspace_size(B, H, 512, num_splits), dtype=torch.uint8,
+                                device=q_cat.device)
+    _check(lib().mla_decode_sparse_fp8(_dtype_code(o_lat_out, q_cat), as_mla_tensor(o_lat_out), _ptr(lse_out),
+                                       as_mla_tensor(q_cat), as_mla_tensor(cache), _ptr(indices),
+                                       indices.stride(0) if indices.dim() == 2 else 0, indices.shape[-1],
+                                       softmax_scale, num_splits, workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def mla_prefill_workspace_size(batch: int) -> int:

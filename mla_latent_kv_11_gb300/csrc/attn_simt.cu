@@ -75,7 +75,9 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   return before;
 }
 
+// A null length array gives every sequence cap rows (a sparse query's index list).
 __device__ __forceinline__ int clamp_len(const int32_t* seq_lens, int b, int cap) {
+  if (seq_lens == nullptr) return cap;
   int n = seq_lens[b];
   if (n < 0 || n > cap) {
     atomicOr(&g_attn_err, kErrDeviceData);
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     if (b < B) {
       s.piece_base[b] = carry + ex;
       // everything a tensor-core walker needs about b in one 16-byte load
-      const int len = min(max(seq_lens[b], 0), cap);
+      const int len = seq_lens == nullptr ? cap : min(max(seq_lens[b], 0), cap);
       s.seqinfo[b] = make_int4(pre[b], len, np, carry + ex - fu);
     }
     __syncthreads();
@@ -235,6 +237,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
 // (odd pitch: a warp reading one column of 32 rows hits 32 banks), then the
 // probabilities and the per-head softmax state.
 struct SimtSmem {
+  int64_t* kbase;   // [kKeys] offset of each staged key row's first element (-1: not attended)
   float* q;
   float* k;
   float (*p)[kKeys];
@@ -246,13 +249,15 @@ struct SimtSmem {
 
 __host__ __device__ inline size_t simt_smem_bytes(int E) {
   const int pitch = E + 1;
-  return sizeof(float) * ((size_t)(kHeads + kKeys) * pitch + kHeads * kKeys + 3 * kHeads);
+  return sizeof(int64_t) * kKeys +
+         sizeof(float) * ((size_t)(kHeads + kKeys) * pitch + kHeads * kKeys + 3 * kHeads);
 }
 
 __device__ inline SimtSmem simt_smem(unsigned char* raw, int E) {
   SimtSmem s;
   s.pitch = E + 1;
-  float* f = reinterpret_cast<float*>(raw);
+  s.kbase = reinterpret_cast<int64_t*>(raw);
+  float* f = reinterpret_cast<float*>(s.kbase + kKeys);
   s.q = f;
   s.k = s.q + kHeads * s.pitch;
   s.p = reinterpret_cast<float(*)[kKeys]>(s.k + kKeys * s.pitch);
@@ -262,13 +267,61 @@ __device__ inline SimtSmem simt_smem(unsigned char* raw, int E) {
   return s;
 }
 
-// K is the cache's element type (T, or e4m3 codes as uint8_t); the query is multiplied by
-// dq and every cache value by dk as they are staged (the dequantisation of an fp8 cache; 1 else).
-template <typename T, typename K>
+// Where the key rows of one query come from. row(t) gives the element offset of the query's
+// t-th row (-1 if that row is not attended; a bad block id or slot is reported too) and
+// at(base, e) the value of its element e.
+//
+// Paged rows of a sequence: row t sits in block bt_row[t / page] at row t % page; K is the
+// cache's element type (T, or e4m3 codes read as value * dk).
+template <typename K>
+struct PagedRows {
+  const K* cache;
+  CacheView cv;
+  const int32_t* bt_row;
+  float dk;
+  __device__ int64_t row(int t) const {
+    const int blk = bt_row[t / cv.page];
+    if (blk < 0 || blk >= cv.num_blocks) {
+      atomicOr(&g_attn_err, kErrDeviceData);
+      return -1;
+    }
+    return (int64_t)blk * cv.s_blk + (int64_t)(t % cv.page) * cv.s_row;
+  }
+  __device__ float at(int64_t base, int e) const { return ld(cache + base + e) * dk; }
+};
+
+// The listed slots of a sparse query over a ds_mla cache (656-byte entries: 512 e4m3 latent
+// codes, four float32 scales each covering 128 latent columns, 64 bf16 rope values): row t is
+// slot idx_row[t] (block slot / page, row slot % page); negative slots are padding.
+struct DsMlaRows {
+  const uint8_t* cache;   // byte addressed
+  int64_t s_blk, s_row;   // bytes
+  int32_t page;
+  int64_t num_rows;
+  const int32_t* idx_row;
+  __device__ int64_t row(int t) const {
+    const int slot = idx_row[t];
+    if (slot < 0) return -1;
+    if (slot >= num_rows) {
+      atomicOr(&g_attn_err, kErrDeviceData);
+      return -1;
+    }
+    return (int64_t)(slot / page) * s_blk + (int64_t)(slot % page) * s_row;
+  }
+  __device__ float at(int64_t base, int e) const {
+    const uint8_t* p = cache + base;
+    if (e < kDsMlaLatent)
+      return ld(p + e) * *reinterpret_cast<const float*>(p + kDsMlaLatent + 4 * (e / kDsMlaGroup));
+    return ld(reinterpret_cast<const __nv_bfloat16*>(p + kDsMlaRopeByte) + (e - kDsMlaLatent));
+  }
+};
+
+// Rows [k0, k1) of one query through the row source; the query is multiplied by dq as it is
+// staged (the dequantisation of an fp8 query scale; 1 else).
+template <typename T, typename Rows>
 __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int64_t q_s_head,
-                            int h0, int hn, int E, int L, const CacheView& cv,
-                            const int32_t* __restrict__ bt_row, int k0, int k1, float scale,
-                            float (&acc)[kHeads][2], float dq = 1.f, float dk = 1.f) {
+                            int h0, int hn, int E, int L, const Rows& rows, int k0, int k1, float scale,
+                            float (&acc)[kHeads][2], float dq = 1.f) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = sm.pitch;
   __syncthreads();  // the previous segment's epilogue may still read m and l
@@ -282,22 +335,15 @@ __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int
   }
 #pragma unroll
   for (int h = 0; h < kHeads; ++h) acc[h][0] = acc[h][1] = 0.f;
-  const K* cache = static_cast<const K*>(cv.data);
   for (int kt = k0; kt < k1; kt += kKeys) {
     __syncthreads();
-    // stage key rows kt .. kt+31 (rows past k1 are zero and masked below)
+    // where key rows kt .. kt+31 live (rows past k1 and unattended rows: -1, zero and masked)
+    if (tid < kKeys) sm.kbase[tid] = kt + tid < k1 ? rows.row(kt + tid) : -1;
+    __syncthreads();
     for (int i = tid; i < kKeys * E; i += kThreads) {
       const int j = i / E, e = i - j * E;
-      const int t = kt + j;
-      float v = 0.f;
-      if (t < k1) {
-        const int blk = bt_row[t / cv.page];
-        if (blk >= 0 && blk < cv.num_blocks)
-          v = ld(cache + (int64_t)blk * cv.s_blk + (int64_t)(t % cv.page) * cv.s_row + e) * dk;
-        else if (e == 0)
-          atomicOr(&g_attn_err, kErrDeviceData);
-      }
-      sm.k[j * P + e] = v;
+      const int64_t base = sm.kbase[j];
+      sm.k[j * P + e] = base >= 0 ? rows.at(base, e) : 0.f;
     }
     __syncthreads();
     // scores: warp w owns heads 2w, 2w+1; lane owns key kt + lane
@@ -305,7 +351,7 @@ __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int
       const int h = 2 * warp + hh;
       float s = 0.f;
       for (int e = 0; e < E; ++e) s = fmaf(sm.q[h * P + e], sm.k[lane * P + e], s);
-      s = (kt + lane < k1) ? s * scale : -CUDART_INF_F;
+      s = sm.kbase[lane] >= 0 ? s * scale : -CUDART_INF_F;
       float mx = s;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -346,17 +392,44 @@ __device__ void attend_rows(const SimtSmem& sm, const T* __restrict__ q_row, int
   __syncthreads();
 }
 
-template <typename T, typename K>
+// The row sources of the split kernel, one per query: a paged sequence through its block-table
+// row, or a sparse query's index list.
+template <typename K>
+struct PagedSource {
+  CacheView cv;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const float* descale_k;
+  __device__ PagedRows<K> rows(int b) const {
+    return PagedRows<K>{static_cast<const K*>(cv.data), cv, block_table + (int64_t)b * bt_stride,
+                        descale_k != nullptr ? *descale_k : 1.f};
+  }
+};
+
+struct DsMlaSource {
+  const uint8_t* cache;
+  int64_t s_blk, s_row;
+  int32_t page;
+  int64_t num_rows;
+  const int32_t* indices;
+  int64_t idx_stride;
+  __device__ DsMlaRows rows(int b) const {
+    return DsMlaRows{cache, s_blk, s_row, page, num_rows, indices + (int64_t)b * idx_stride};
+  }
+};
+
+// One work unit's tile range: every sequence segment in it is attended by attend_rows and
+// written whole (o_lat, lse) or as a partial slot for the combine. A null seq_lens gives every
+// query cap rows.
+template <typename T, typename Source>
 __global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
     T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
-    const T* __restrict__ q, int64_t q_s0, int64_t q_s1, CacheView cv,
-    const int32_t* __restrict__ block_table, int64_t bt_stride,
+    const T* __restrict__ q, int64_t q_s0, int64_t q_s1, Source src,
     const int32_t* __restrict__ seq_lens, int cap, int B, int H, int L, int R, float scale,
-    DecodeSched s, const float* __restrict__ descale_q, const float* __restrict__ descale_k) {
+    DecodeSched s, const float* __restrict__ descale_q) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   pdl_enter();
   const float dq = descale_q != nullptr ? *descale_q : 1.f;
-  const float dk = descale_k != nullptr ? *descale_k : 1.f;
   const SimtSmem sm = simt_smem(smem_raw, L + R);
   const int w = blockIdx.x;
   const int t0 = s.unit_tile[w], t1 = s.unit_tile[w + 1];
@@ -374,11 +447,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_simt_kernel(
   for (int t = t0; t < t1;) {
     while (s.tile_prefix[b + 1] <= t) ++b;
     const int seg_end = min(t1, s.tile_prefix[b + 1]);
-    const int len = min(max(seq_lens[b], 0), cap);
+    const int len = seq_lens == nullptr ? cap : min(max(seq_lens[b], 0), cap);
     const int k0 = (t - s.tile_prefix[b]) * kTile;
     const int k1 = min((seg_end - s.tile_prefix[b]) * kTile, len);
-    attend_rows<T, K>(sm, q + (int64_t)b * q_s0, q_s1, h0, hn, E, L, cv,
-                      block_table + (int64_t)b * bt_stride, k0, k1, scale, acc, dq, dk);
+    attend_rows(sm, q + (int64_t)b * q_s0, q_s1, h0, hn, E, L, src.rows(b), k0, k1, scale, acc, dq);
     const bool whole = s.npieces[b] == 1;
     const int slot = whole ? 0 : s.piece_base[b] + (w - s.first_unit[b]);
     for (int h = 0; h < hn; ++h) {
@@ -586,8 +658,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(
   int end = 0;
   if (i >= 0 && i < q_len) end = min(kv, max(0, kv - q_len + i + 1));
   float acc[kHeads][2];
-  attend_rows<T, T>(sm, q + (int64_t)r * q_s0, q_s1, h0, hn, L + R, L, cv,
-                 block_table + (int64_t)b * bt_stride, 0, end, scale, acc);
+  const PagedRows<T> rows{static_cast<const T*>(cv.data), cv, block_table + (int64_t)b * bt_stride, 1.f};
+  attend_rows(sm, q + (int64_t)r * q_s0, q_s1, h0, hn, L + R, L, rows, 0, end, scale, acc);
   for (int h = 0; h < hn; ++h) {
     const float l = sm.l[h];
     const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -618,37 +690,57 @@ cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t m
   return launch_k(decode_schedule_kernel, 1, threads, 0, st, seq_lens, B, (int)(cap > INT32_MAX ? INT32_MAX : cap), s);
 }
 
+namespace {
+template <typename T, typename Source>
+cudaError_t launch_split_simt(const View3& o_lat, float* lse, const View3& q, const Source& src,
+                              const int32_t* seq_lens, int cap, int32_t B, int32_t H, int32_t L, int32_t R,
+                              float scale, const DecodeSched& s, const float* descale_q, cudaStream_t st) {
+  const dim3 grid(s.units, (H + kHeads - 1) / kHeads);
+  const size_t sm = simt_smem_bytes(L + R);
+  allow_smem(decode_split_simt_kernel<T, Source>, sm);
+  return launch_k(decode_split_simt_kernel<T, Source>, grid, kThreads, sm, st, (T*)o_lat.data, o_lat.s0,
+                  o_lat.s1, lse, (const T*)q.data, q.s0, q.s1, src, seq_lens, cap, B, H, L, R, scale, s,
+                  descale_q);
+}
+
+template <typename T>
+cudaError_t launch_paged_simt(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
+                              const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens, int cap,
+                              int32_t B, int32_t H, int32_t L, int32_t R, float scale, const DecodeSched& s,
+                              cudaStream_t st, bool fp8_cache, const float* descale_q, const float* descale_k) {
+  if (fp8_cache)
+    return launch_split_simt<T>(o_lat, lse, q, PagedSource<uint8_t>{cache, block_table, bt_stride, descale_k},
+                                seq_lens, cap, B, H, L, R, scale, s, descale_q, st);
+  return launch_split_simt<T>(o_lat, lse, q, PagedSource<T>{cache, block_table, bt_stride, descale_k}, seq_lens,
+                              cap, B, H, L, R, scale, s, descale_q, st);
+}
+}  // namespace
+
 cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
                                const CacheView& cache, const int32_t* block_table,
                                int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t H,
                                int32_t L, int32_t R, float scale, const DecodeSched& s,
                                cudaStream_t st, bool fp8_cache, const float* descale_q, const float* descale_k) {
-  const dim3 grid(s.units, (H + kHeads - 1) / kHeads);
   const long long cap_ll = (long long)max_blocks * cache.page;
   const int cap = (int)(cap_ll > INT32_MAX ? INT32_MAX : cap_ll);
-  const size_t sm = simt_smem_bytes(L + R);
-  if (dt == MLA_F32) {
-    if (fp8_cache) {
-      allow_smem(decode_split_simt_kernel<float, uint8_t>, sm);
-      return launch_k(decode_split_simt_kernel<float, uint8_t>, grid, kThreads, sm, st,
-          (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
-          block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
-    }
-    allow_smem(decode_split_simt_kernel<float, float>, sm);
-    return launch_k(decode_split_simt_kernel<float, float>, grid, kThreads, sm, st,
-        (float*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const float*)q.data, q.s0, q.s1, cache,
-        block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
-  }
-  if (fp8_cache) {
-    allow_smem(decode_split_simt_kernel<__nv_bfloat16, uint8_t>, sm);
-    return launch_k(decode_split_simt_kernel<__nv_bfloat16, uint8_t>, grid, kThreads, sm, st,
-        (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
-        q.s1, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
-  }
-  allow_smem(decode_split_simt_kernel<__nv_bfloat16, __nv_bfloat16>, sm);
-  return launch_k(decode_split_simt_kernel<__nv_bfloat16, __nv_bfloat16>, grid, kThreads, sm, st,
-      (__nv_bfloat16*)o_lat.data, o_lat.s0, o_lat.s1, lse, (const __nv_bfloat16*)q.data, q.s0,
-      q.s1, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale, s, descale_q, descale_k);
+  if (dt == MLA_F32)
+    return launch_paged_simt<float>(o_lat, lse, q, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R, scale,
+                                    s, st, fp8_cache, descale_q, descale_k);
+  return launch_paged_simt<__nv_bfloat16>(o_lat, lse, q, cache, block_table, bt_stride, seq_lens, cap, B, H, L, R,
+                                          scale, s, st, fp8_cache, descale_q, descale_k);
+}
+
+cudaError_t launch_decode_sparse_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
+                                      const DsMlaCache& cache, const int32_t* indices, int64_t idx_stride,
+                                      int32_t topk, int32_t B, int32_t H, float scale, const DecodeSched& s,
+                                      cudaStream_t st) {
+  const DsMlaSource src{static_cast<const uint8_t*>(cache.data), cache.s_blk, cache.s_row, cache.page,
+                        (int64_t)cache.num_blocks * cache.page, indices, idx_stride};
+  if (dt == MLA_F32)
+    return launch_split_simt<float>(o_lat, lse, q, src, nullptr, topk, B, H, kDsMlaLatent, kDsMlaRope, scale, s,
+                                    nullptr, st);
+  return launch_split_simt<__nv_bfloat16>(o_lat, lse, q, src, nullptr, topk, B, H, kDsMlaLatent, kDsMlaRope, scale,
+                                          s, nullptr, st);
 }
 
 cudaError_t launch_decode_combine(mla_dtype dt, const View3& o_lat, float* lse,

@@ -446,6 +446,49 @@ mla_status mla_decode_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out,
                     workspace, lay, (cudaStream_t)stream, true, descale_q, descale_k);
 }
 
+mla_status mla_decode_sparse_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
+                                 mla_tensor cache, const int32_t* indices, int64_t indices_stride,
+                                 int32_t topk, float softmax_scale, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat, 3, "q_cat"));
+  MLA_TRY(check_view(o_lat_out, 3, "o_lat_out"));
+  const int64_t B = q_cat.shape[0], H = q_cat.shape[1];
+  if (q_cat.shape[2] != kDsMlaLatent + kDsMlaRope)
+    return fail(MLA_ERR_INVALID_ARG, "q_cat width %lld, a ds_mla query is 576 wide", (long long)q_cat.shape[2]);
+  if (o_lat_out.shape[0] != B || o_lat_out.shape[1] != H || o_lat_out.shape[2] != kDsMlaLatent)
+    return fail(MLA_ERR_INVALID_ARG, "o_lat_out must be [B,H,512] = [%lld,%lld,512]", (long long)B, (long long)H);
+  MLA_TRY(check_cache(cache, kDsMlaEntry, "cache"));
+  if (reinterpret_cast<uintptr_t>(cache.data) % 16 != 0 || cache.stride[0] % 16 != 0 || cache.stride[1] % 16 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "cache: data and strides must be 16-byte aligned");
+  if (cache.shape[0] * cache.shape[1] > INT32_MAX)
+    return fail(MLA_ERR_UNSUPPORTED, "cache: more slots than an int32 index can name");
+  if (topk < 0) return fail(MLA_ERR_INVALID_ARG, "topk < 0");
+  if (num_splits < 0) return fail(MLA_ERR_INVALID_ARG, "num_splits < 0");
+  if (B == 0 || H == 0) return MLA_OK;
+  if (B > INT32_MAX / 2 || H > 4096) return fail(MLA_ERR_UNSUPPORTED, "batch or head count too large");
+  if (topk > 0 && (indices == nullptr || indices_stride < topk))
+    return fail(MLA_ERR_INVALID_ARG, "indices must be non-null with a row stride >= topk");
+  const int32_t units = decode_units(num_splits);
+  const DecodeWsLayout lay = decode_ws_layout(B, H, kDsMlaLatent, units);
+  if (workspace == nullptr || workspace_bytes < lay.total)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes, lay.total);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const cudaStream_t st = (cudaStream_t)stream;
+  const DecodeSched s = decode_sched_from_ws(workspace, lay, (int32_t)B, units);
+  const DsMlaCache cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0], (int32_t)cache.shape[1]};
+  const View3 ov = view3(o_lat_out), qv = view3(q_cat);
+  // every query has topk listed rows: the schedule's lengths are all topk (cap topk, page 1)
+  MLA_TRY(cuda_status(launch_decode_schedule(nullptr, (int32_t)B, topk, 1, s, st), "mla_decode_sparse_fp8 schedule"));
+  MLA_TRY(cuda_status(launch_decode_sparse_simt(dtype, ov, lse_out, qv, cv, indices, indices_stride, topk,
+                                                (int32_t)B, (int32_t)H, softmax_scale, s, st),
+                      "mla_decode_sparse_fp8 split kernel"));
+  return cuda_status(launch_decode_combine(dtype, ov, lse_out, nullptr, (int32_t)B, (int32_t)H, kDsMlaLatent, s, st),
+                     "mla_decode_sparse_fp8 combine");
+}
+
 size_t mla_prefill_workspace_size(int32_t batch) {
   if (batch < 0) return 0;
   return ((size_t)(batch + 1) * sizeof(int32_t) + 255) & ~size_t(255);

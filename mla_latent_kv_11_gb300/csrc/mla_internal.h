@@ -19,6 +19,22 @@ constexpr unsigned kErrTimeout = 2u;     // a bounded wait gave up
 // Keys per schedule tile of the split-KV decode (one page of 64 rows at page 64).
 constexpr int kTile = 64;
 
+// The fp8 ds_mla cache entry: e4m3 latent codes, then float32 scales (one per group of
+// latent columns), then bf16 rope values.
+constexpr int kDsMlaLatent = 512;
+constexpr int kDsMlaGroup = 128;
+constexpr int kDsMlaRope = 64;
+constexpr int kDsMlaRopeByte = kDsMlaLatent + 4 * (kDsMlaLatent / kDsMlaGroup);   // 528
+constexpr int kDsMlaEntry = kDsMlaRopeByte + 2 * kDsMlaRope;                       // 656
+static_assert(kDsMlaEntry == MLA_DS_MLA_ENTRY_BYTES, "ds_mla entry layout");
+
+// A ds_mla cache view: entry (blk, row) at data + blk*s_blk + row*s_row bytes.
+struct DsMlaCache {
+  const void* data;
+  int64_t s_blk, s_row;
+  int32_t num_blocks, page;
+};
+
 // A rank-3 strided view in ELEMENTS (data already includes the storage offset).
 struct View3 {
   void* data;
@@ -120,6 +136,12 @@ cudaError_t launch_decode_simt(mla_dtype dt, const View3& o_lat, float* lse, con
                                int32_t L, int32_t R, float scale, const DecodeSched& s,
                                cudaStream_t st, bool fp8_cache = false, const float* descale_q = nullptr,
                                const float* descale_k = nullptr);
+// Sparse top-k decode over a ds_mla cache (split kernel only: schedule and combine as above,
+// the schedule run with null lengths and cap = topk).
+cudaError_t launch_decode_sparse_simt(mla_dtype dt, const View3& o_lat, float* lse, const View3& q,
+                                      const DsMlaCache& cache, const int32_t* indices, int64_t idx_stride,
+                                      int32_t topk, int32_t B, int32_t H, float scale, const DecodeSched& s,
+                                      cudaStream_t st);
 // e4m3 cache write: codes of x / (*scale) (float32, correctly rounded), round to nearest even,
 // saturating; src_dt is kv_c's and k_pe's element type.
 cudaError_t launch_cache_write_fp8(mla_dtype src_dt, const View3& cache, const View3& kv_c, const View3& k_pe,
