@@ -686,7 +686,7 @@ def decode_figures(mla, mi, device, out, peaks, timed) -> None:
             nbytes8 = decode_algorithmic_bytes([ctx] * B, B, H, L, R, nbl, cache_es=1)
             out["decode_fp8_b64_ctx8192_fixed"] = {
                 "ms": ms8, "gbs": nbytes8 / (ms8 * 1e-3) / 1e9, "queries_per_s": B / (ms8 * 1e-3),
-                "path": "CUDA-core split kernel (e4m3 rows converted on load)",
+                "path": "tensor cores (e4m3 rows gathered and converted to bf16 in shared memory)",
                 "roofline": roofline(nbytes8, flops, ms8, peaks)}
             del cache8, rows, slots
         del cache, q, o, ws

@@ -218,8 +218,12 @@ mla_status mla_decode_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out,
  *   and k_pe the bf16 rope values; the softmax and outputs as mla_decode. A query
  *   with no valid slot gets o = 0, lse = -inf. A slot past the cache is skipped and
  *   reported by mla_device_error (MLA_ERR_DEVICE_DATA).
- *   num_splits, workspace: as mla_decode, sized by
- *   mla_decode_workspace_size(B, H, 512, num_splits). */
+ *   num_splits: as mla_decode; workspace: device scratch of at least
+ *   mla_decode_sparse_workspace_size(B, H, topk, num_splits) bytes, 256-byte
+ *   aligned, caller-owned. */
+/* Bytes of workspace mla_decode_sparse_fp8 needs. */
+size_t mla_decode_sparse_workspace_size(int32_t batch, int32_t num_heads, int32_t topk, int32_t num_splits);
+
 mla_status mla_decode_sparse_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
                                  mla_tensor cache, const int32_t* indices, int64_t indices_stride,
                                  int32_t topk, float softmax_scale, int32_t num_splits, void* workspace,

@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "mla_decode_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, P, P, I32, P, SZ, P],
                                ctypes.c_int),
             "mla_decode_sparse_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, F32, I32, P, SZ, P], ctypes.c_int),
+            "mla_decode_sparse_workspace_size": ([I32, I32, I32, I32], SZ),
             "mla_device_error": ([P], ctypes.c_int),
             "mla_check_bounded_wait": ([ctypes.c_uint32, P], ctypes.c_int),
         }
@@ -258,6 +259,10 @@ def mla_decode_fp8(o_lat_out, q_cat, cache, block_table, seq_lens, kv_lora_rank:
                                 _stream(stream)))
 
 
+def mla_decode_sparse_workspace_size(batch: int, num_heads: int, topk: int, num_splits: int = 0) -> int:
+    return int(lib().mla_decode_sparse_workspace_size(batch, num_heads, topk, num_splits))
+
+
 def mla_decode_sparse_fp8(o_lat_out, q_cat, cache, indices, softmax_scale: float, lse_out=None,
                           num_splits: int = 0, workspace=None, stream=None) -> None:
     """Sparse top-k decode over an fp8 ds_mla cache: query b attends the slots indices[b]
@@ -276,8 +281,8 @@ def mla_decode_sparse_fp8(o_lat_out, q_cat, cache, indices, softmax_scale: float
         raise MlaError(MLA_ERR_INVALID_ARG, "lse_out must be contiguous float32")
     B, H = q_cat.shape[0], q_cat.shape[1]
     if workspace is None:
-        workspace = torch.empty(mla_decode_workspace_size(B, H, 512, num_splits), dtype=torch.uint8,
-                                device=q_cat.device)
+        workspace = torch.empty(mla_decode_sparse_workspace_size(B, H, indices.shape[-1], num_splits),
+                                dtype=torch.uint8, device=q_cat.device)
     _check(lib().mla_decode_sparse_fp8(_dtype_code(o_lat_out, q_cat), as_mla_tensor(o_lat_out), _ptr(lse_out),
                                        as_mla_tensor(q_cat), as_mla_tensor(cache), _ptr(indices),
                                        indices.stride(0) if indices.dim() == 2 else 0, indices.shape[-1],

@@ -673,6 +673,31 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(
   }
 }
 
+// A sparse query's index list, compacted: its valid slots (0 <= slot < num_rows) in listed
+// order and their count; a slot past the cache is dropped and reported. One warp a query.
+__global__ void __launch_bounds__(256) sparse_compact_kernel(const int32_t* __restrict__ idx, int64_t idx_stride,
+                                                             int topk, int B, int64_t num_rows,
+                                                             int32_t* __restrict__ out, int32_t* __restrict__ counts) {
+  pdl_enter();
+  const int q = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (q >= B) return;
+  const int32_t* row = idx + (int64_t)q * idx_stride;
+  int32_t* o = out + (int64_t)q * topk;
+  int n = 0;
+  for (int base = 0; base < topk; base += 32) {
+    const int t = base + lane;
+    int slot = t < topk ? row[t] : -1;
+    if (slot >= num_rows) {
+      atomicOr(&g_attn_err, kErrDeviceData);
+      slot = -1;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, slot >= 0);
+    if (slot >= 0) o[n + __popc(m & ((1u << lane) - 1u))] = slot;
+    n += __popc(m);
+  }
+  if (lane == 0) counts[q] = n;
+}
+
 template <typename K>
 void allow_smem(K k, size_t bytes) {
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -774,6 +799,13 @@ cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, co
         q.s1, cache, block_table, bt_stride, max_blocks, cu_q, kv_lens, B, H, L, R, scale);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_compact(const int32_t* indices, int64_t idx_stride, int32_t topk, int32_t B,
+                                  int64_t num_rows, int32_t* out, int32_t* counts, cudaStream_t st) {
+  const int blocks = (int)((B + 7) / 8);
+  return launch_k(sparse_compact_kernel, blocks, 256, 0, st, indices, idx_stride, (int)topk, (int)B, num_rows, out,
+                  counts);
 }
 
 unsigned attn_simt_errors_read_clear() {

@@ -91,6 +91,8 @@ constexpr int kXchgWarp0 = 4;             // exchange warpgroup: warps 4..7
 constexpr int kSoftmaxWarp0 = 8;          // softmax warpgroup: warps 8..11
 constexpr int kSoftmaxBar = 1;            // named barrier of the softmax warpgroup
 constexpr int kXchgBar = 2;               // named barrier of the exchange warpgroup
+constexpr int kLoadBar = 3;               // named barrier of the loader warps (e4m3 caches)
+constexpr int kLoaders = 64;              // loader threads: warps 0 and 2
 constexpr float kLazyRescale = 8.0f;      // log2 units
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
@@ -100,15 +102,26 @@ constexpr uint32_t kTmemQ = 352;
 constexpr uint32_t kTmemL = 496;          // row sums of P, accumulated by the tensor core (16 equal columns)
 constexpr int kOnesBytes = 16 * kKeysT * 2;   // a 16 x 64 tile of bf16 ones: B operand of the row-sum MMA
 
-template <int kRope>
+// kSrc: where a CTA's key tile comes from. 0: bf16 cache rows, TMA-loaded as swizzled boxes.
+// 1: e4m3 cache rows through the block table, 2: fp8 ds_mla entries at a query's (compacted)
+// slots; both gathered by cp.async into a staging ring and converted to bf16 in the layout the
+// TMA would have written.
+template <int kRope, int kSrc>
 struct Cfg {
-  static constexpr int kStages = 5;
+  static constexpr int kStages = kSrc ? 3 : 5;
   static constexpr int kStageBytes = 4 * kBoxBytesK + (kRope ? kRopeBoxBytes : 0);
+  // staged 16-byte granules of one row: 16 latent + 2 rope (e4m3), or 16 latent + the four
+  // scales + 4 rope (ds_mla: the rope is bf16)
+  static constexpr int kGran = kSrc == 1 ? 16 + (kRope ? 2 : 0) : kSrc == 2 ? 21 : 0;
+  static constexpr int kStg = kSrc ? 3 : 0;
+  static constexpr int kStgBytes = kKeysT * kGran * 16;
   static constexpr int kOffKV = 0;
   static constexpr int kOffOnes = kOffKV + kStages * kStageBytes;   // 1 KB aligned: stages are
   static constexpr int kOffXloc = kOffOnes + kOnesBytes;            // own E + c of a tile: 2 pieces
   static constexpr int kOffXrem = kOffXloc + 2 * kXSlot;            // the peer's pieces: a ring of 3
-  static constexpr int kOffBar = (kOffXrem + kInSlots * kXSlot + 127) & ~127;
+  static constexpr int kOffStg = kOffXrem + kInSlots * kXSlot;      // staging ring (16-byte aligned)
+  static constexpr int kOffRowBase = kOffStg + kStg * kStgBytes;    // [2][64] row offsets of a tile
+  static constexpr int kOffBar = (kOffRowBase + (kSrc ? 2 * kKeysT * 8 : 0) + 127) & ~127;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmem = kOffBar + kBarBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;    // slack for 1 KB alignment
@@ -126,6 +139,8 @@ struct Bars {
   uint64_t x_full[kInSlots];   // the peer's piece has landed in incoming slot i
   uint64_t x_empty[kInSlots];  // the peer has read its incoming slot i (arrived on by the peer)
   uint64_t xin_free[kInSlots]; // the softmax group has read incoming slot i
+  // gathered (e4m3) tiles: staging slot u holds the raw bytes of a tile, and is free again
+  uint64_t stg_full[3], stg_empty[3];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -146,6 +161,12 @@ __device__ long long g_trace_all[2][304][8][128];
     if (unit == 0 && (g) < 512) g_trace[rank][ev][(g)] = now_;                        \
     if (blockIdx.x < 304 && (g) < 128) g_trace_all[0][blockIdx.x][ev][(g)] = now_;    \
   } while (0)
+// loader events of work unit 0 (e4m3 caches)
+__device__ long long g_trace3[2][8][512];
+#define MLA_TRACE3_AT(ev, g)                                                   \
+  do {                                                                          \
+    if (unit == 0 && lt == 0 && (g) < 512) g_trace3[rank][ev][(g)] = clock64(); \
+  } while (0)
 #define MLA_TRACE2_AT(ev, g)                                                                  \
   do {                                                                                         \
     const long long now_ = clock64();                                                          \
@@ -157,6 +178,9 @@ __device__ long long g_trace_all[2][304][8][128];
   do {                      \
   } while (0)
 #define MLA_TRACE2_AT(ev, g) \
+  do {                       \
+  } while (0)
+#define MLA_TRACE3_AT(ev, g) \
   do {                       \
   } while (0)
 #endif
@@ -191,6 +215,14 @@ struct TcParams {
   const int32_t* seq_lens;
   int B;
   DecodeSched sched;
+  // e4m3 rows (byte strides): kSrc 1 through the block table with descale_q / descale_k
+  // (null: 1) folded into the scores and the output; kSrc 2 at slots[b * slot_stride + t]
+  const uint8_t* cache8;
+  int64_t s_blk8, s_row8;
+  const float* descale_q;
+  const float* descale_k;
+  const int32_t* slots;
+  int64_t slot_stride;
   // prefill
   const int32_t* cu_q;
   const int32_t* kv_lens;
@@ -270,6 +302,43 @@ __device__ __forceinline__ float exp2_int(float d) {
   return d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
 }
 
+// Four e4m3 codes (one word, low byte first) -> their values as fp32. A code's exponent and
+// mantissa bits placed in an fp32's exponent and mantissa fields read as value * 2^-120 (an fp32
+// subnormal for exponent 0, which the multiply honours), so one multiply by 2^120 gives every
+// finite value exactly; the sign bit goes to bit 31 first. `mul` may carry a further factor.
+__device__ __forceinline__ void e4m3x4_values(uint32_t x, float mul, float (&f)[4]) {
+  f[0] = __uint_as_float(((x << 24) & 0x80000000u) | ((x << 20) & 0x07F00000u)) * 0x1p120f * mul;
+  f[1] = __uint_as_float(((x << 16) & 0x80000000u) | ((x << 12) & 0x07F00000u)) * 0x1p120f * mul;
+  f[2] = __uint_as_float(((x << 8) & 0x80000000u) | ((x << 4) & 0x07F00000u)) * 0x1p120f * mul;
+  f[3] = __uint_as_float((x & 0x80000000u) | ((x >> 4) & 0x07F00000u)) * 0x1p120f * mul;
+  // the two NaN codes (all exponent and mantissa bits set) are rare: patched here
+  if ((((x & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (((x >> (8 * k)) & 0x7Fu) == 0x7Fu) f[k] = __uint_as_float(0x7FC00000u);
+  }
+}
+
+// 16 codes -> 16 bf16 (eight words, low value first): exact (truncating an fp32 that holds an
+// e4m3 value exactly), or with a scale each product rounded to nearest.
+template <bool kScaled>
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 w, float sc, uint32_t (&o)[8]) {
+  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float f[4];
+    e4m3x4_values(wv[k], kScaled ? sc : 1.f, f);
+    if (kScaled) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
+      o[2 * k] = *reinterpret_cast<const uint32_t*>(&a);
+      o[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b);
+    } else {
+      o[2 * k] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632);
+      o[2 * k + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632);
+    }
+  }
+}
+
 __device__ __forceinline__ int ntiles(const Seg& s) { return (s.k1 - s.k0 + kKeysT - 1) / kKeysT; }
 
 __device__ __forceinline__ void set_abort(Bars& bars, uint32_t peer) {
@@ -279,11 +348,12 @@ __device__ __forceinline__ void set_abort(Bars& bars, uint32_t peer) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(1) : "memory");
 }
 
-template <int kRope>
+template <int kRope, int kSrc>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_attn_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap ropemap,
                        const TcParams p) {
-  using C = Cfg<kRope>;
+  using C = Cfg<kRope, kSrc>;
+  static_assert(kSrc == 0 || kSrc == 1 || (kSrc == 2 && kRope == 64), "a ds_mla entry has a 64-wide rope part");
   static_assert(sizeof(Bars) <= C::kBarBytes, "barrier block overflows its slot");
   static_assert(C::kSmemAlloc <= 232448, "shared memory beyond the 227 KB a CTA may hold");
   static_assert(C::kStages <= 8, "kv barrier arrays hold 8 stages");
@@ -304,8 +374,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_full[s], kSrc ? kLoaders : 1);
       mbar_init(&bars.kv_empty[s], 1);
+    }
+    for (int u = 0; u < C::kStg; ++u) {
+      mbar_init(&bars.stg_full[u], kLoaders);
+      mbar_init(&bars.stg_empty[u], kLoaders);
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.s_empty, 4);
@@ -331,7 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars.tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (kSrc == 0 && warp == 0 && lane == 0) {
     tma_prefetch_desc(&kvmap);
     if (kRope) tma_prefetch_desc(&ropemap);
   }
@@ -344,6 +418,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   pdl_enter();      // the queries, the cache and the schedule come from the kernels before
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort_flag;
+
 #ifdef MLA_TRACE
   if (tid == 0 && blockIdx.x < 512) {
     uint32_t smid;
@@ -354,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 #endif
 
-  if (warp == 0) {
+  if (kSrc == 0 && warp == 0) {
     // ------------------------------------------------------------ TMA producer (cache tiles)
     Walker wk;
     wk.init(p, unit, nunits);
@@ -429,6 +504,131 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int s = 0; s < C::kStages; ++s)
         if (issued[s] > 0 && !mbar_wait(&bars.kv_full[s], (issued[s] - 1) & 1, &dummy))
           atomicOr(&g_tc_err, kErrTimeout);   // a copy that never landed: report, never pass silently
+    }
+  } else if (kSrc != 0 && (warp == 0 || warp == 2)) {
+    if constexpr (kSrc != 0) {
+      // ------------------------------------------------------------ loader (e4m3 caches): 64
+      // threads gather this CTA's bytes of every key row with cp.async into a staging slot (rows
+      // past the segment are zero-filled), running up to kStg tiles ahead, and convert each landed
+      // tile to bf16 in the swizzled layout of a TMA box once its bf16 stage is free
+      const int lt = (warp == 0 ? 0 : 32) + lane;
+      constexpr int G = C::kGran;
+      constexpr int GC = kSrc == 1 ? G : 20;     // granules converted per row (the scales are read)
+      auto group_all = [](bool v) { return named_bar_and(kLoadBar, kLoaders, v); };
+      int64_t* rowbase = reinterpret_cast<int64_t*>(smem + C::kOffRowBase);
+      unsigned char* stg = smem + C::kOffStg;
+      Walker wk;
+      wk.init(p, unit, nunits);
+      Seg sg;
+      int nt = 0, j = 0;           // tiles of the current segment, next tile in it
+      bool have = false;           // a segment is open
+      int gi = 0, gc = 0;          // tiles issued, tiles converted
+      bool ok = true, more = true;
+      while (ok) {
+        // ---- issue: up to kStg tiles ahead of the conversion
+        while (ok && more && gi < gc + C::kStg) {
+          while (!have || j >= nt) {
+            if (!wk.next(p, sg)) {
+              more = false;
+              break;
+            }
+            nt = ntiles(sg);
+            j = 0;
+            have = true;
+          }
+          if (!more) break;
+          const int u = gi % C::kStg;
+          MLA_TRACE3_AT(0, gi);
+          ok = group_all(mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort));
+          if (!ok) break;
+          // byte offset of each row of the tile (-1: past the segment or a bad block id)
+          int64_t* rb = rowbase + (gi & 1) * kKeysT;
+          {
+            const int t = sg.k0 + j * kKeysT + lt;
+            int64_t off = -1;
+            if (t < sg.k1) {
+              if (kSrc == 1) {
+                const int blk = p.block_table[(int64_t)sg.b * p.bt_stride + t / p.page];
+                if (blk >= 0 && blk < p.num_blocks)
+                  off = (int64_t)blk * p.s_blk8 + (int64_t)(t % p.page) * p.s_row8;
+                else
+                  atomicOr(&g_tc_err, kErrDeviceData);
+              } else {
+                const int slot = p.slots[(int64_t)sg.b * p.slot_stride + t];   // compacted: in range
+                off = (int64_t)(slot / p.page) * p.s_blk8 + (int64_t)(slot % p.page) * p.s_row8;
+              }
+            }
+            rb[lt] = off;
+          }
+          named_bar(kLoadBar, kLoaders);
+          MLA_TRACE3_AT(1, gi);
+          const uint32_t dst0 = smem_u32(stg + u * C::kStgBytes);
+          for (int f = lt; f < kKeysT * G; f += kLoaders) {
+            const int r = f / G, g = f - r * G;
+            const int64_t off = rb[r];
+            int byte;
+            if (kSrc == 1)
+              byte = g < 16 ? col0 + 16 * g : 512 + kRopeHalf * (int)rank + 16 * (g - 16);
+            else
+              byte = g < 16 ? col0 + 16 * g : g == 16 ? kDsMlaLatent : kDsMlaRopeByte + 64 * (int)rank + 16 * (g - 17);
+            cp_async16(dst0 + f * 16, p.cache8 + (off < 0 ? 0 : off + byte), off < 0 ? 0u : 16u);
+          }
+          cp_async_commit();
+          cp_async_arrive_noinc(&bars.stg_full[u]);
+          MLA_TRACE3_AT(2, gi);
+          ++gi;
+          ++j;
+        }
+        if (!ok || gc == gi) break;
+        // ---- convert tile gc: staging slot u -> bf16 stage s
+        const int u = gc % C::kStg, s = gc % C::kStages;
+        MLA_TRACE3_AT(3, gc);
+        ok = mbar_wait(&bars.stg_full[u], (gc / C::kStg) & 1, abort);
+        MLA_TRACE3_AT(4, gc);
+        ok = group_all(ok && mbar_wait(&bars.kv_empty[s], ((gc / C::kStages) & 1) ^ 1, abort));
+        MLA_TRACE3_AT(5, gc);
+        if (!ok) break;
+        const unsigned char* src = stg + u * C::kStgBytes;
+        unsigned char* dst = sKV + s * C::kStageBytes;
+        for (int f = lt; f < kKeysT * GC; f += kLoaders) {
+          const int r = f / GC, g = f - r * GC;
+          const unsigned char* row = src + r * G * 16;
+          if (g < 16) {
+            // 16 latent codes -> 16 bf16: two 16-byte chunks of box g / 4
+            const uint4 w = *reinterpret_cast<const uint4*>(row + g * 16);
+            uint32_t o[8];
+            if (kSrc == 1)
+              e4m3x16_to_bf16<false>(w, 1.f, o);
+            else
+              e4m3x16_to_bf16<true>(w, reinterpret_cast<const float*>(row + 16 * 16)[2 * (int)rank + g / 8], o);
+            unsigned char* bx = dst + (g >> 2) * kBoxBytesK + r * 128;
+            const int j0 = (g & 3) * 2;
+            *reinterpret_cast<uint4*>(bx + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          } else {
+            // rope: 64-byte rows of the rope box, 64-byte swizzle
+            unsigned char* bx = dst + 4 * kBoxBytesK + r * 64;
+            if (kSrc == 1) {
+              uint32_t o[8];
+              e4m3x16_to_bf16<false>(*reinterpret_cast<const uint4*>(row + g * 16), 1.f, o);
+              const int j0 = (g - 16) * 2;
+              *reinterpret_cast<uint4*>(bx + ((j0 ^ ((r >> 1) & 3)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ ((r >> 1) & 3)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+              const int jr = g - 16;   // bf16 already: one chunk, from staged granule 17 + jr
+              *reinterpret_cast<uint4*>(bx + ((jr ^ ((r >> 1) & 3)) << 4)) =
+                  *reinterpret_cast<const uint4*>(row + (17 + jr) * 16);
+            }
+          }
+        }
+        fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
+        mbar_arrive(&bars.kv_full[s]);
+        mbar_arrive(&bars.stg_empty[u]);
+        MLA_TRACE3_AT(6, gc);
+        ++gc;
+      }
+      cp_async_wait_all();   // never leave with copies in flight
+      if (!ok) set_abort(bars, peer);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer. The whole
@@ -689,7 +889,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.s_empty);
-        // ---- own row max c (base 2, scale folded in) and E = 2^(x - c) in bf16
+        // ---- own row max c (base 2, scale folded in) and E = 2^(x - c) in bf16. The bf16 path's
+        // scale is positive (checked on the host), so max(s) * scale is the maximum of x; an e4m3
+        // cache's descales are device values of either sign, so there x is formed first
+        float xs = p.scale_log2;
+        if (kSrc == 1) {
+          // an e4m3 cache's descales: the scores scale by descale_q * descale_k
+          const float dq = p.descale_q != nullptr ? *p.descale_q : 1.f;
+          const float dk = p.descale_k != nullptr ? *p.descale_k : 1.f;
+          const float sl2 = p.scale_log2 * (dq * dk);
+#pragma unroll
+          for (int k = 0; k < 64; ++k) sv[k] *= sl2;
+          xs = 1.f;
+        }
         const int kbase = sg.k0 + j * kKeysT;
         if (!__all_sync(0xffffffffu, kbase + kKeysT <= limit)) {
 #pragma unroll
@@ -703,7 +915,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float c = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         // rounded up to an integer: still an upper bound, and it makes every factor
         // 2^(M - m) of the softmax an exact power of two
-        c = c == -CUDART_INF_F ? -CUDART_INF_F : ceilf(c * p.scale_log2);
+        c = c == -CUDART_INF_F ? -CUDART_INF_F : ceilf(c * xs);
         const float neg_c = c == -CUDART_INF_F ? 0.f : -c;
         // ---- each half: E of its 32 keys into its piece, then straight to the peer, so the
         // first piece is on its way while the second is computed
@@ -712,8 +924,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t ek[16];
 #pragma unroll
           for (int k = 0; k < 32; k += 2) {
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(ex2_approx(fmaf(sv[32 * h + k], p.scale_log2, neg_c)),
-                                                            ex2_approx(fmaf(sv[32 * h + k + 1], p.scale_log2, neg_c)));
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(ex2_approx(fmaf(sv[32 * h + k], xs, neg_c)),
+                                                            ex2_approx(fmaf(sv[32 * h + k + 1], xs, neg_c)));
             ek[k >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
           }
           unsigned char* piece = sXloc + h * kXSlot;
@@ -859,7 +1071,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // rows of a partial tile past the sequence: zero their V so garbage cannot reach O
         const int kbase = sg.k0 + j * kKeysT;
         const int nvalid = sg.k1 - kbase;
-        if (nvalid < kKeysT) {
+        if (kSrc == 0 && nvalid < kKeysT) {   // gathered tiles were zero-filled past the segment
           unsigned char* st = sKV + (g % C::kStages) * C::kStageBytes;
           const int per_box = (kKeysT - nvalid) * 8;         // 16-byte chunks per latent box
           for (int i = row; i < 4 * per_box; i += 128) {
@@ -888,7 +1100,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         l = lv[0];
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // an e4m3 cache's values scale by descale_k
+      const float out_mul = kSrc == 1 && p.descale_k != nullptr ? *p.descale_k : 1.f;
+      const float inv = l > 0.f ? out_mul / l : 0.f;
       const int tok = sg.tok0 + t_in_tile;
       for (int c = 0; c < 256; c += 32) {
         float v[32];
@@ -969,7 +1183,7 @@ __global__ void prefill_items_kernel(const int32_t* __restrict__ cu_q, int B, in
   }
 }
 
-template <int kRope>
+template <int kRope, int kSrc = 0>
 int max_clusters() {
   static std::mutex mu;
   static std::vector<int> cache;
@@ -978,8 +1192,9 @@ int max_clusters() {
   std::lock_guard<std::mutex> g(mu);
   if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
   if (cache[dev] == 0) {
-    using C = Cfg<kRope>;
-    cudaFuncSetAttribute(mla_attn_tc_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+    using C = Cfg<kRope, kSrc>;
+    cudaFuncSetAttribute(mla_attn_tc_kernel<kRope, kSrc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         C::kSmemAlloc);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * device_sm_count(), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -992,7 +1207,7 @@ int max_clusters() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mla_attn_tc_kernel<kRope>, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, mla_attn_tc_kernel<kRope, kSrc>, &cfg) != cudaSuccess || n <= 0)
       n = device_sm_count() / 2;
     cudaGetLastError();
     cache[dev] = n;
@@ -1000,14 +1215,15 @@ int max_clusters() {
   return cache[dev];
 }
 
-template <int kRope>
+template <int kRope, int kSrc>
 cudaError_t launch_tc(const TcParams& p, const CUtensorMap& km, const CUtensorMap& rm, int clusters,
                       cudaStream_t st) {
-  using C = Cfg<kRope>;
-  cudaError_t e = cudaFuncSetAttribute(mla_attn_tc_kernel<kRope>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using C = Cfg<kRope, kSrc>;
+  cudaError_t e = cudaFuncSetAttribute(mla_attn_tc_kernel<kRope, kSrc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  return launch_k(mla_attn_tc_kernel<kRope>, dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st, km, rm, p);
+  return launch_k(mla_attn_tc_kernel<kRope, kSrc>, dim3(2 * clusters), dim3(kThreads), C::kSmemAlloc, st, km, rm,
+                  p);
 }
 
 }  // namespace
@@ -1064,7 +1280,7 @@ bool tc_attention_supported(mla_dtype dt, int H, int L, int R, bool decode, cons
 }
 
 int tc_decode_units(int num_splits) {
-  return num_splits > 0 ? num_splits : max_clusters<64>();
+  return num_splits > 0 ? num_splits : max_clusters<64, 0>();
 }
 
 static cudaError_t run_tc(mla_dtype, TcParams& p, const View3& q, const CacheView& cv, int clusters,
@@ -1079,11 +1295,11 @@ static cudaError_t run_tc(mla_dtype, TcParams& p, const View3& q, const CacheVie
   if (!make_map3d(&km, cv.data, E, cv.page, cv.num_blocks, (uint64_t)cv.s_row * 2, (uint64_t)cv.s_blk * 2, 64,
                   rows_box, 1, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (p.R == 0) return launch_tc<0>(p, km, km, clusters, st);
+  if (p.R == 0) return launch_tc<0, 0>(p, km, km, clusters, st);
   if (!make_map3d(&rm, cv.data, E, cv.page, cv.num_blocks, (uint64_t)cv.s_row * 2, (uint64_t)cv.s_blk * 2,
                   kRopeHalf, rows_box, 1, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  return launch_tc<64>(p, km, rm, clusters, st);
+  return launch_tc<64, 0>(p, km, rm, clusters, st);
 }
 
 cudaError_t launch_decode_tc(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
@@ -1113,6 +1329,76 @@ cudaError_t launch_decode_tc(const View3& o_lat, float* lse, const View3& q, con
   return run_tc(MLA_BF16, p, q, cache, s.units, st);
 }
 
+namespace {
+TcParams decode_params(const View3& o_lat, float* lse, const View3& q, int32_t B, int32_t H, int32_t R, float scale,
+                       const DecodeSched& s) {
+  TcParams p{};
+  p.mode = 0;
+  p.H = H;
+  p.tpt = kRows / H;
+  p.L = 512;
+  p.R = R;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q = static_cast<const __nv_bfloat16*>(q.data);
+  p.q_s0 = q.s0;
+  p.q_s1 = q.s1;
+  p.o_lat = static_cast<__nv_bfloat16*>(o_lat.data);
+  p.o_s0 = o_lat.s0;
+  p.o_s1 = o_lat.s1;
+  p.lse = lse;
+  p.B = B;
+  p.sched = s;
+  return p;
+}
+}  // namespace
+
+bool tc_gather_supported(mla_dtype dt, int H, const void* cache, int64_t s_blk_bytes, int64_t s_row_bytes,
+                         const View3& q, const View3& o) {
+  if (dt != MLA_BF16 || (H != 128 && H != 64)) return false;
+  auto al16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
+  if (!al16(cache) || s_blk_bytes % 16 || s_row_bytes % 16) return false;
+  if (!al16(q.data) || q.s0 % 8 || q.s1 % 8) return false;
+  if (!al16(o.data) || o.s0 % 8 || o.s1 % 8) return false;
+  return true;
+}
+
+cudaError_t launch_decode_tc_fp8(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
+                                 const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                 int32_t B, int32_t H, int32_t R, float scale, const float* descale_q,
+                                 const float* descale_k, const DecodeSched& s, cudaStream_t st) {
+  TcParams p = decode_params(o_lat, lse, q, B, H, R, scale, s);
+  p.page = cache.page;
+  p.num_blocks = cache.num_blocks;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  const long long cap = (long long)max_blocks * cache.page;
+  p.cap = (int)(cap > 0x3fffffff ? 0x3fffffff : cap);
+  p.cache8 = static_cast<const uint8_t*>(cache.data);
+  p.s_blk8 = cache.s_blk;
+  p.s_row8 = cache.s_row;
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  CUtensorMap none{};
+  if (R == 0) return launch_tc<0, 1>(p, none, none, s.units, st);
+  return launch_tc<64, 1>(p, none, none, s.units, st);
+}
+
+cudaError_t launch_decode_tc_dsmla(const View3& o_lat, float* lse, const View3& q, const DsMlaCache& cache,
+                                   const int32_t* slots, int64_t slot_stride, int32_t topk, int32_t B, int32_t H,
+                                   float scale, const DecodeSched& s, cudaStream_t st) {
+  TcParams p = decode_params(o_lat, lse, q, B, H, kDsMlaRope, scale, s);
+  p.page = cache.page;
+  p.num_blocks = cache.num_blocks;
+  p.cap = topk;
+  p.cache8 = static_cast<const uint8_t*>(cache.data);
+  p.s_blk8 = cache.s_blk;
+  p.s_row8 = cache.s_row;
+  p.slots = slots;
+  p.slot_stride = slot_stride;
+  CUtensorMap none{};
+  return launch_tc<64, 2>(p, none, none, s.units, st);
+}
+
 cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
                               const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                               const int32_t* cu_q, const int32_t* kv_lens, int32_t B, int32_t H, int32_t L,
@@ -1140,7 +1426,7 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
   p.item_prefix = item_prefix;
   cudaError_t e = launch_k(prefill_items_kernel, 1, 32, 0, st, cu_q, B, p.tpt, item_prefix);
   if (e != cudaSuccess) return e;
-  const int clusters = R == 64 ? max_clusters<64>() : max_clusters<0>();
+  const int clusters = R == 64 ? max_clusters<64, 0>() : max_clusters<0, 0>();
   return run_tc(MLA_BF16, p, q, cache, clusters, st);
 }
 
@@ -1150,6 +1436,9 @@ extern "C" int mla_debug_trace(long long* host) {
   if (!e) e = (int)cudaMemcpyFromSymbol(host + 2 * 8 * 512, g_trace2, sizeof(g_trace2));
   if (!e) e = (int)cudaMemcpyFromSymbol(host + 4 * 8 * 512, g_cta_time, sizeof(g_cta_time));
   if (!e) e = (int)cudaMemcpyFromSymbol(host + 4 * 8 * 512 + 512 * 10, g_trace_all, sizeof(g_trace_all));
+  if (!e)
+    e = (int)cudaMemcpyFromSymbol(host + 4 * 8 * 512 + 512 * 10 + sizeof(g_trace_all) / 8, g_trace3,
+                                  sizeof(g_trace3));
   return e;
 }
 #endif

@@ -280,7 +280,11 @@ mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, con
   const DecodeSched s = decode_sched_from_ws(scratch, lay, (int32_t)dc.B, dc.units);
   const int32_t B = (int32_t)dc.B, H = (int32_t)dc.H, L = (int32_t)dc.L, R = (int32_t)dc.R;
   MLA_TRY(cuda_status(launch_decode_schedule(seq_lens, B, max_blocks, dc.cv.page, s, st), "mla_decode schedule"));
-  if (dc.tc) {
+  if (dc.tc && fp8_cache) {
+    MLA_TRY(cuda_status(launch_decode_tc_fp8(dc.ov, lse_out, dc.qv, dc.cv, block_table, block_table_stride,
+                                             max_blocks, B, H, R, softmax_scale, descale_q, descale_k, s, st),
+                        "mla_decode split kernel (tensor cores, e4m3 cache)"));
+  } else if (dc.tc) {
     MLA_TRY(cuda_status(launch_decode_tc(dc.ov, lse_out, dc.qv, dc.cv, block_table, block_table_stride,
                                          max_blocks, seq_lens, B, H, L, R, softmax_scale, s, st),
                         "mla_decode split kernel (tensor cores)"));
@@ -434,8 +438,10 @@ mla_status mla_decode_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out,
   MLA_TRY(check_decode_args(dtype, o_lat_out, q_cat, cache, block_table, block_table_stride, max_blocks,
                             seq_lens, kv_lora_rank, rope_dim, softmax_scale, num_splits, &dc));
   if (dc.empty) return MLA_OK;
-  dc.tc = false;   // the e4m3 cache is read by the general kernel
-  dc.units = decode_units(num_splits);
+  // the tensor-core kernel gathers e4m3 rows with 16-byte copies and converts them to bf16
+  dc.tc = softmax_scale > 0.f && dc.L == 512 && (dc.R == 0 || dc.R == 64) &&
+          tc_gather_supported(dtype, (int)dc.H, dc.cv.data, dc.cv.s_blk, dc.cv.s_row, dc.qv, dc.ov);
+  dc.units = dc.tc ? tc_decode_units(num_splits) : decode_units(num_splits);
   const DecodeWsLayout lay = decode_ws_layout(dc.B, dc.H, dc.L, decode_units(num_splits));
   if (workspace == nullptr || workspace_bytes < lay.total)
     return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes,
@@ -444,6 +450,29 @@ mla_status mla_decode_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out,
     return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   return run_decode(dtype, dc, lse_out, block_table, block_table_stride, max_blocks, seq_lens, softmax_scale,
                     workspace, lay, (cudaStream_t)stream, true, descale_q, descale_k);
+}
+
+namespace {
+// The sparse decode's workspace: mla_decode's layout, then the compacted slots [B, topk] and
+// their counts [B].
+struct SparseWs {
+  DecodeWsLayout lay;
+  size_t off_slots, off_counts, total;
+};
+SparseWs sparse_ws(int64_t B, int64_t H, int64_t topk, int32_t units) {
+  SparseWs w;
+  w.lay = decode_ws_layout(B, H, kDsMlaLatent, units);
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  w.off_slots = up(w.lay.total);
+  w.off_counts = up(w.off_slots + (size_t)B * (size_t)topk * 4);
+  w.total = up(w.off_counts + (size_t)B * 4);
+  return w;
+}
+}  // namespace
+
+size_t mla_decode_sparse_workspace_size(int32_t batch, int32_t num_heads, int32_t topk, int32_t num_splits) {
+  if (batch < 0 || num_heads < 0 || topk < 0 || num_splits < 0) return 0;
+  return sparse_ws(batch, num_heads, topk, decode_units(num_splits)).total;
 }
 
 mla_status mla_decode_sparse_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* lse_out, mla_tensor q_cat,
@@ -470,21 +499,37 @@ mla_status mla_decode_sparse_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* l
   if (B > INT32_MAX / 2 || H > 4096) return fail(MLA_ERR_UNSUPPORTED, "batch or head count too large");
   if (topk > 0 && (indices == nullptr || indices_stride < topk))
     return fail(MLA_ERR_INVALID_ARG, "indices must be non-null with a row stride >= topk");
-  const int32_t units = decode_units(num_splits);
-  const DecodeWsLayout lay = decode_ws_layout(B, H, kDsMlaLatent, units);
-  if (workspace == nullptr || workspace_bytes < lay.total)
-    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes, lay.total);
+  const SparseWs ws = sparse_ws(B, H, topk, decode_units(num_splits));
+  if (workspace == nullptr || workspace_bytes < ws.total)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes, ws.total);
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   const cudaStream_t st = (cudaStream_t)stream;
-  const DecodeSched s = decode_sched_from_ws(workspace, lay, (int32_t)B, units);
   const DsMlaCache cv{cache.data, cache.stride[0], cache.stride[1], (int32_t)cache.shape[0], (int32_t)cache.shape[1]};
   const View3 ov = view3(o_lat_out), qv = view3(q_cat);
-  // every query has topk listed rows: the schedule's lengths are all topk (cap topk, page 1)
-  MLA_TRY(cuda_status(launch_decode_schedule(nullptr, (int32_t)B, topk, 1, s, st), "mla_decode_sparse_fp8 schedule"));
-  MLA_TRY(cuda_status(launch_decode_sparse_simt(dtype, ov, lse_out, qv, cv, indices, indices_stride, topk,
-                                                (int32_t)B, (int32_t)H, softmax_scale, s, st),
-                      "mla_decode_sparse_fp8 split kernel"));
+  const bool tc = softmax_scale > 0.f && topk > 0 &&
+                  tc_gather_supported(dtype, (int)H, cache.data, cache.stride[0], cache.stride[1], qv, ov);
+  const int32_t units = tc ? tc_decode_units(num_splits) : decode_units(num_splits);
+  const DecodeSched s = decode_sched_from_ws(workspace, ws.lay, (int32_t)B, units);
+  if (tc) {
+    // the tensor-core kernel takes each query's valid slots, compacted, as a sequence of
+    // count rows
+    int32_t* slots = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + ws.off_slots);
+    int32_t* counts = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + ws.off_counts);
+    MLA_TRY(cuda_status(launch_sparse_compact(indices, indices_stride, topk, (int32_t)B,
+                                              (int64_t)cv.num_blocks * cv.page, slots, counts, st),
+                        "mla_decode_sparse_fp8 slot compaction"));
+    MLA_TRY(cuda_status(launch_decode_schedule(counts, (int32_t)B, topk, 1, s, st), "mla_decode_sparse_fp8 schedule"));
+    MLA_TRY(cuda_status(launch_decode_tc_dsmla(ov, lse_out, qv, cv, slots, topk, topk, (int32_t)B, (int32_t)H,
+                                               softmax_scale, s, st),
+                        "mla_decode_sparse_fp8 split kernel (tensor cores)"));
+  } else {
+    // every query has topk listed rows: the schedule's lengths are all topk (cap topk, page 1)
+    MLA_TRY(cuda_status(launch_decode_schedule(nullptr, (int32_t)B, topk, 1, s, st), "mla_decode_sparse_fp8 schedule"));
+    MLA_TRY(cuda_status(launch_decode_sparse_simt(dtype, ov, lse_out, qv, cv, indices, indices_stride, topk,
+                                                  (int32_t)B, (int32_t)H, softmax_scale, s, st),
+                        "mla_decode_sparse_fp8 split kernel"));
+  }
   return cuda_status(launch_decode_combine(dtype, ov, lse_out, nullptr, (int32_t)B, (int32_t)H, kDsMlaLatent, s, st),
                      "mla_decode_sparse_fp8 combine");
 }

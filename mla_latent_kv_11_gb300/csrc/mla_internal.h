@@ -142,6 +142,22 @@ cudaError_t launch_decode_sparse_simt(mla_dtype dt, const View3& o_lat, float* l
                                       const DsMlaCache& cache, const int32_t* indices, int64_t idx_stride,
                                       int32_t topk, int32_t B, int32_t H, float scale, const DecodeSched& s,
                                       cudaStream_t st);
+// The valid slots of each sparse query in listed order ([B, topk], compacted) and their counts.
+cudaError_t launch_sparse_compact(const int32_t* indices, int64_t idx_stride, int32_t topk, int32_t B,
+                                  int64_t num_rows, int32_t* out, int32_t* counts, cudaStream_t st);
+// Tensor-core decode over gathered e4m3 rows (attn_tc.cu): bf16 queries, 64 or 128 heads, a
+// 16-byte aligned cache with 16-byte strides, 16-byte aligned query and output views.
+bool tc_gather_supported(mla_dtype dt, int H, const void* cache, int64_t s_blk_bytes, int64_t s_row_bytes,
+                         const View3& q, const View3& o);
+// An e4m3 paged cache (rope 0 or 64, L = 512).
+cudaError_t launch_decode_tc_fp8(const View3& o_lat, float* lse, const View3& q, const CacheView& cache,
+                                 const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                 int32_t B, int32_t H, int32_t R, float scale, const float* descale_q,
+                                 const float* descale_k, const DecodeSched& s, cudaStream_t st);
+// A ds_mla cache at compacted slots (the schedule ran on their counts, cap topk).
+cudaError_t launch_decode_tc_dsmla(const View3& o_lat, float* lse, const View3& q, const DsMlaCache& cache,
+                                   const int32_t* slots, int64_t slot_stride, int32_t topk, int32_t B, int32_t H,
+                                   float scale, const DecodeSched& s, cudaStream_t st);
 // e4m3 cache write: codes of x / (*scale) (float32, correctly rounded), round to nearest even,
 // saturating; src_dt is kv_c's and k_pe's element type.
 cudaError_t launch_cache_write_fp8(mla_dtype src_dt, const View3& cache, const View3& kv_c, const View3& k_pe,

@@ -161,6 +161,20 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// ---------------------------------------------------------------- gathered copies
+// 16 bytes global -> shared through L2 (cp.async.cg); `src_bytes` < 16 fills the rest of the
+// 16 bytes with zeros (0: nothing is read, all zeros).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed (the arrival is
+// counted in the barrier's expected count: .noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Bulk copy of `bytes` from this CTA's shared memory to `dst` in a peer CTA's shared
 // memory; completion is counted in bytes on the peer's mbarrier `mbar` (both are
 // shared::cluster addresses). The copy joins this thread's bulk async-group.

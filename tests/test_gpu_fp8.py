@@ -150,3 +150,78 @@ def test_fp8_write_then_decode_round_trip(mla):
     want, _ = orc.decode_fp8(mi.decode_f64(q_bits, "bf16"), st, 0, page, (page * E, E, 1), L, R, table,
                              np.array(lens), 1.0 / math.sqrt(192), 1.0, 0.25)
     check_close(to_f64(o), want, "bf16", "fp8 write then decode")
+
+
+@pytest.mark.parametrize("H,R,page,dq,dk", [(128, 64, 16, -0.5, 2.0), (64, 0, 128, 1.0, 0.25),
+                                           (64, 64, 64, 2.0, -1.0), (128, 0, 64, 1.0, 1.0)],
+                         ids=["h128_page16_neg_dq", "h64_nope_page128", "h64_rope_neg_dk", "h128_nope"])
+def test_fp8_decode_bf16_queries_geometries_and_descale_signs(mla, H, R, page, dq, dk):
+    # the bf16-query decode over e4m3 rows at other head counts, rope widths and page sizes, with
+    # descales of either sign (the score scale is then negative: the row maximum must follow)
+    import torch
+    L = 512
+    E = L + R
+    lens = [0, 1, 64, 65, 333, 1500, 63]
+    codes, table = _fp8_batch(H, L, R, lens, page, 7401 + H + R + page, abs(dk))
+    q_bits = mi.encode(mi.draw("normal", 7410 + H + R, len(lens) * H * E, 0.5), "bf16").reshape(len(lens), H, E)
+    scale = 1.0 / math.sqrt(E)
+    want, want_lse = orc.decode_fp8(mi.decode_f64(q_bits, "bf16"), codes.reshape(-1), 0, page, (page * E, E, 1),
+                                    L, R, table, np.array(lens), scale, dq, dk)
+    o = poisoned((len(lens), H, L), "bf16")
+    lse = torch.full((len(lens), H), float("nan"), dtype=torch.float32, device="cuda")
+    mla.mla_decode_fp8(o, to_dev(q_bits, "bf16"), _u8(codes), torch.from_numpy(table).cuda(),
+                       torch.from_numpy(np.array(lens, np.int32)).cuda(), L, R, scale,
+                       descale_q=torch.tensor([dq], dtype=torch.float32, device="cuda"),
+                       descale_k=torch.tensor([dk], dtype=torch.float32, device="cuda"), lse_out=lse)
+    mla.mla_device_error()
+    check_close(to_f64(o), want, "bf16", f"fp8 decode H={H} R={R} page={page}")
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(got_lse), fin)
+    assert np.max(np.abs(got_lse[fin] - want_lse[fin])) < 1e-2
+    assert np.all(to_f64(o)[0] == 0)
+
+
+def test_fp8_decode_single_row_reads_every_code_exactly(mla):
+    # one cached row holding every finite code: with one key the softmax weight is 1, so o_lat is
+    # that row's values, which bf16 holds exactly (subnormals and signs included; -0 reads as 0
+    # after the weighted sum)
+    import torch
+    H, L, R, page = 128, 512, 64, 64
+    E = L + R
+    codes = np.arange(256, dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0                         # no NaN codes in a score
+    row = np.concatenate([codes, codes[::-1], np.full(R, 0x38, np.uint8)])   # rope: 1.0
+    cache = np.zeros((2, page, E), np.uint8)
+    cache[1, 0] = row
+    table = np.array([[1]], np.int32)
+    q_bits = mi.encode(mi.draw("normal", 7501, H * E, 0.1), "bf16").reshape(1, H, E)
+    o = poisoned((1, H, L), "bf16")
+    mla.mla_decode_fp8(o, to_dev(q_bits, "bf16"), _u8(cache), torch.from_numpy(table).cuda(),
+                       torch.tensor([1], dtype=torch.int32, device="cuda"), L, R, 0.1)
+    mla.mla_device_error()
+    want = orc.e4m3_value(row[:L])
+    got = to_f64(o)[0]
+    assert np.array_equal(got, np.broadcast_to(want, (H, L)))
+
+
+def test_sparse_decode_single_slot_reads_every_code_exactly(mla):
+    # the ds_mla entry of one slot with every finite code and power-of-two scales: o_lat is the
+    # products, exactly
+    import torch
+    H = 64
+    codes = np.arange(256, dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0
+    lat = np.concatenate([codes, codes[::-1]])
+    scales = np.array([1.0, 0.5, 2.0, 0.25], "<f4")
+    rope = mi.to_bf16_bits(mi.normal(7502, 64) * np.float32(0.1))
+    entry = np.concatenate([lat, scales.view(np.uint8), rope.astype("<u2").view(np.uint8)])
+    cache = np.zeros((3, 16, 656), np.uint8)
+    cache[2, 5] = entry
+    q_bits = mi.encode(mi.draw("normal", 7503, H * 576, 0.1), "bf16").reshape(1, H, 576)
+    o = poisoned((1, H, 512), "bf16")
+    mla.mla_decode_sparse_fp8(o, to_dev(q_bits, "bf16"), _u8(cache),
+                              torch.tensor([[-1, 2 * 16 + 5, -1]], dtype=torch.int32, device="cuda"), 0.1)
+    mla.mla_device_error()
+    want = orc.ds_mla_values(entry[None, :])[0][0]
+    assert np.array_equal(to_f64(o)[0], np.broadcast_to(want, (H, 512)))
