@@ -4,15 +4,16 @@ A step is one decode step of the large V3 workload: 64 sequences, 128 heads,
 context lengths drawn uniformly from [1024, 16384], page 64, random block
 table; bf16 storage, fp32 accumulation. One step runs every stage of the path
 through the C ABI: absorb (W_UK fold) -> q concat and cache write of the new
-rows (one launch) -> split-KV decode (schedule, split kernel, LSE combine) ->
-v_up (W_UV).
+rows (one launch) -> split-KV decode with the W_UV un-projection (schedule,
+split kernel, LSE combine fused with v_up).
 Inputs are resident in HBM before the timed region; the latent cache (about
 0.56 GB) is larger than L2 (129 MB), so no flush is needed between steps.
 
 Printed (rank 0, one JSON line): value = latent-KV GB/s, i.e. the decode
 stage's algorithmic bytes (cache rows read, q_cat read, o_lat written, block
 table and lengths read) per step over the step time; queries/s beside it; the
-roofline of the decode call (timed live with CUDA events on its stream); the
+roofline of the decode-and-un-project call (timed live with CUDA events on its
+stream, with that call's own algorithmic bytes and flops); the
 end-to-end figure through the same API with host buffers; the float64 oracle
 timed on a bounded sample on the host cores; and the SM clocks sampled during
 the timed region.
@@ -66,6 +67,14 @@ def decode_algorithmic_bytes(seq_lens, B, H, L, R, max_blocks, es=2, cache_es=No
 
 def decode_algorithmic_flops(seq_lens, H, L, R) -> int:
     return int(sum(int(n) for n in seq_lens)) * H * 2 * ((L + R) + L)
+
+
+def decode_v_up_algorithmic(seq_lens, B, H, L, R, V, es=2) -> tuple[int, int]:
+    """Bytes and flops of the decode with its un-projection as one call: the decode's, less
+    the o_lat it no longer writes, plus W_UV read and out written; plus the un-projection's
+    2*B*H*L*V flops."""
+    nbytes = decode_algorithmic_bytes(seq_lens, B, H, L, R, 0, es) - B * H * L * es + H * L * V * es + B * H * V * es
+    return nbytes, decode_algorithmic_flops(seq_lens, H, L, R) + 2 * B * H * L * V
 
 
 def roofline(nbytes: float, flops: float, ms: float, peaks: dict, sustained: bool = False) -> dict:
@@ -147,8 +156,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _traffic_for(kernel_src: str) -> float | None:
-    """ncu DRAM bytes per launch recorded for the current source of the kernel, else None."""
+TRAFFIC_SOURCES = ("attn_tc.cu", "attn_simt.cu", "combine_vup.cu")
+
+
+def _sources_sha(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "mla_latent_kv_11_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_for(names=TRAFFIC_SOURCES) -> float | None:
+    """ncu DRAM bytes per call recorded for the current sources of its kernels, else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -156,8 +175,10 @@ def _traffic_for(kernel_src: str) -> float | None:
     entry = d.get("decode")
     if not entry:
         return None
-    src = open(os.path.join(ROOT, "mla_latent_kv_11_gb300", "csrc", kernel_src), "rb").read()
-    if hashlib.sha256(src).hexdigest()[:16] != entry.get("source_sha"):
+    try:
+        if _sources_sha(names) != entry.get("source_sha"):
+            return None
+    except OSError:
         return None
     return float(entry["bytes_per_launch"])
 
@@ -165,7 +186,7 @@ def _traffic_for(kernel_src: str) -> float | None:
 # --------------------------------------------------------------------------- the workload
 
 class DecodeStep:
-    """Device-resident inputs of one decode step and the four calls that run it."""
+    """Device-resident inputs of one decode step and the three calls that run it."""
 
     def __init__(self, mla, w, device, rank_seed=0):
         import numpy as np
@@ -192,11 +213,11 @@ class DecodeStep:
         self.cache = dev(w.full_cache())
         B, H, L, E, V = self.B, self.H, self.L, self.E, self.V
         self.q_cat = torch.empty((B, H, E), dtype=dt, device=device)
-        self.o_lat = torch.empty((B, H, L), dtype=dt, device=device)
         self.out = torch.empty((B, H, V), dtype=dt, device=device)
-        self.ws = torch.empty(mla.mla_decode_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
-        # absorb (1) + concat and cache write (1) + decode (schedule, split, combine: 3) + v_up (1)
-        self.launches_per_step = 6
+        self.ws = torch.empty(mla.mla_decode_v_up_workspace_size(B, H, L, 0), dtype=torch.uint8, device=device)
+        # absorb (1) + concat and cache write (1) + decode with v_up (schedule, split, combine
+        # with the un-projection: 3)
+        self.launches_per_step = 5
 
     def run(self, ev_decode=None, q_nope=None, q_pe=None, kv_c=None, k_pe=None, slots=None,
             table=None, lens=None, out=None):
@@ -213,11 +234,11 @@ class DecodeStep:
                                    self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
         if ev_decode is not None:
             ev_decode[0].record()
-        m.mla_decode(self.o_lat, self.q_cat, self.cache, self.table if table is None else table,
-                     self.lens if lens is None else lens, self.L, self.R, self.w.scale, workspace=self.ws)
+        m.mla_decode_v_up(out, self.q_cat, self.cache, self.table if table is None else table,
+                          self.lens if lens is None else lens, self.L, self.R, self.w.scale, self.w_uv,
+                          workspace=self.ws)
         if ev_decode is not None:
             ev_decode[1].record()
-        m.mla_v_up(out.transpose(0, 1), self.o_lat.transpose(0, 1), self.w_uv)
 
 
 def _smi_id(local: int) -> str:
@@ -398,7 +419,7 @@ def run_ours(args) -> None:
     stream = torch.cuda.current_stream()
     B, H, L, R = step.B, step.H, step.L, step.R
     bytes_step = decode_algorithmic_bytes(w.seq_lens, B, H, L, R, 0)
-    flops_step = decode_algorithmic_flops(w.seq_lens, H, L, R)
+    call_bytes, call_flops = decode_v_up_algorithmic(w.seq_lens, B, H, L, R, step.V)
 
     for _ in range(args.warmup):
         step.run()
@@ -425,7 +446,7 @@ def run_ours(args) -> None:
     clocks = clk.summary()
 
     # end to end through the same calls with host buffers: every step copies its inputs in from
-    # pinned host memory, runs the four calls and copies its output back; like a serving loop,
+    # pinned host memory, runs the three calls and copies its output back; like a serving loop,
     # the copies of neighbouring steps run on two copy streams under the compute (two sets of
     # device buffers, ordered by events), and the timed region ends when the last output is back
     def pinned(t):
@@ -473,7 +494,7 @@ def run_ours(args) -> None:
                  slots=d["slots"], table=d["table"], lens=d["lens"], out=dev_out[b])
 
     # like a serving loop, the step goes to the GPU as one CUDA graph per input buffer set: the
-    # four calls (six kernels) are captured once through the
+    # three calls (five kernels) are captured once through the
     # same C ABI and replayed, so the host's per-call marshalling is paid once, not every step
     for b in range(2):                                 # the first eager runs read real inputs
         dev_buf[b].copy_(host_buf)
@@ -542,7 +563,7 @@ def run_ours(args) -> None:
         return
     peaks = _peaks()
     value = job_throughput(bytes_step, ms_step, world)
-    rl = roofline(bytes_step, flops_step, decode_ms, peaks, sustained=True)
+    rl = roofline(call_bytes, call_flops, decode_ms, peaks, sustained=True)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -552,13 +573,12 @@ def run_ours(args) -> None:
                    "rope_dim": R, "page": w.page, "context": "U[1024,16384] per sequence",
                    "cached_rows": int(w.seq_lens.sum()), "l2": "inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
-        "roofline": {"kernel": "mla_decode (schedule + split + combine)", **rl,
-                     "traffic": _traffic_for("attn_tc.cu") if os.path.exists(
-                         os.path.join(ROOT, "mla_latent_kv_11_gb300", "csrc", "attn_tc.cu")) else None,
+        "roofline": {"kernel": "mla_decode_v_up (schedule + split + combine with the W_UV un-projection)", **rl,
+                     "traffic": _traffic_for(),
                      "peak_source": peaks["source"], "ms_per_launch": decode_ms,
-                     "bytes_per_launch": bytes_step, "flops_per_launch": flops_step,
-                     "hbm_frac": bytes_step / (decode_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                     "tensor_frac": flops_step / (decode_ms * 1e-3) / (peaks["bf16_tflops_sustained"] * 1e12)},
+                     "bytes_per_launch": call_bytes, "flops_per_launch": call_flops,
+                     "hbm_frac": call_bytes / (decode_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "tensor_frac": call_flops / (decode_ms * 1e-3) / (peaks["bf16_tflops_sustained"] * 1e12)},
         "e2e": {"value": job_throughput(bytes_step, e2e_ms, world), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "launch": launch},
         "gpu_launches": step.launches_per_step * args.steps,

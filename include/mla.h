@@ -259,6 +259,29 @@ size_t mla_prefill_workspace_size(int32_t batch);
 mla_status mla_v_up(mla_dtype dtype, mla_tensor out, mla_tensor o_lat, mla_tensor w_uv,
                     void* stream);
 
+/* Steps 4 and 5 as one call - split-KV paged decode whose output goes straight
+ * through the W_UV un-projection ([vt] _v_up_proj at the end of the absorbed
+ * decode; [memra] mla_attn_absorbed -> mla_decompress_v): the LSE combine of the
+ * split sequences and the un-projection run as one kernel, so o_lat is never
+ * written out.
+ *   out [B,H,V] (written; any strides with unit v stride), lse_out device float
+ *   [B,H] or NULL, q_cat, cache, block table, lengths, kv_lora_rank, rope_dim,
+ *   softmax_scale, num_splits: as mla_decode; w_uv [H,L,V] as mla_v_up.
+ *   out[b,h,:] = o_lat[b,h,:] @ w_uv[h] with o_lat the decode's output rounded to
+ *   `dtype` (as mla_decode followed by mla_v_up computes it).
+ *   workspace: device scratch of at least
+ *   mla_decode_v_up_workspace_size(B, H, L, num_splits) bytes, 256-byte aligned,
+ *   caller-owned (it also holds o_lat). Errors: as mla_decode and mla_v_up. */
+mla_status mla_decode_v_up(mla_dtype dtype, mla_tensor out, float* lse_out, mla_tensor q_cat, mla_tensor cache,
+                           const int32_t* block_table, int64_t block_table_stride, int32_t max_blocks,
+                           const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim, float softmax_scale,
+                           mla_tensor w_uv, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Bytes of workspace mla_decode_v_up needs. */
+size_t mla_decode_v_up_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank,
+                                      int32_t num_splits);
+
 /* Bytes of the static scratch behind mla_decode_noalloc (40 MiB). */
 #define MLA_DECODE_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
 

@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
                                ctypes.c_int),
             "mla_decode_sparse_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, F32, I32, P, SZ, P], ctypes.c_int),
             "mla_decode_sparse_workspace_size": ([I32, I32, I32, I32], SZ),
+            "mla_decode_v_up": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, T, I32, P, SZ, P],
+                                ctypes.c_int),
+            "mla_decode_v_up_workspace_size": ([I32, I32, I32, I32], SZ),
             "mla_device_error": ([P], ctypes.c_int),
             "mla_check_bounded_wait": ([ctypes.c_uint32, P], ctypes.c_int),
         }
@@ -288,6 +291,29 @@ def mla_decode_sparse_fp8(o_lat_out, q_cat, cache, indices, softmax_scale: float
                                        indices.stride(0) if indices.dim() == 2 else 0, indices.shape[-1],
                                        softmax_scale, num_splits, workspace.data_ptr(),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def mla_decode_v_up_workspace_size(batch: int, num_heads: int, kv_lora_rank: int, num_splits: int = 0) -> int:
+    return int(lib().mla_decode_v_up_workspace_size(batch, num_heads, kv_lora_rank, num_splits))
+
+
+def mla_decode_v_up(out, q_cat, cache, block_table, seq_lens, kv_lora_rank: int, rope_dim: int,
+                    softmax_scale: float, w_uv, lse_out=None, num_splits: int = 0, workspace=None,
+                    stream=None) -> None:
+    """Steps 4 and 5 as one call: out[b,h,:] = decode(q_cat)[b,h,:] @ w_uv[h]; out [B,H,V], w_uv [H,L,V]."""
+    import torch
+    _check_int32_table(block_table, seq_lens)
+    if lse_out is not None and (lse_out.dtype != torch.float32 or not lse_out.is_contiguous()):
+        raise MlaError(MLA_ERR_INVALID_ARG, "lse_out must be contiguous float32")
+    B, H = q_cat.shape[0], q_cat.shape[1]
+    if workspace is None:
+        workspace = torch.empty(mla_decode_v_up_workspace_size(B, H, kv_lora_rank, num_splits), dtype=torch.uint8,
+                                device=q_cat.device)
+    _check(lib().mla_decode_v_up(_dtype_code(out, q_cat, cache, w_uv), as_mla_tensor(out), _ptr(lse_out),
+                                 as_mla_tensor(q_cat), as_mla_tensor(cache), block_table.data_ptr(),
+                                 block_table.stride(0), block_table.shape[1], seq_lens.data_ptr(), kv_lora_rank,
+                                 rope_dim, softmax_scale, as_mla_tensor(w_uv), num_splits, workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def mla_prefill_workspace_size(batch: int) -> int:

@@ -276,7 +276,7 @@ mla_status check_decode_args(mla_dtype dtype, const mla_tensor& o_lat_out, const
 mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, const int32_t* block_table,
                       int64_t block_table_stride, int32_t max_blocks, const int32_t* seq_lens, float softmax_scale,
                       void* scratch, const DecodeWsLayout& lay, cudaStream_t st, bool fp8_cache,
-                      const float* descale_q, const float* descale_k) {
+                      const float* descale_q, const float* descale_k, bool combine) {
   const DecodeSched s = decode_sched_from_ws(scratch, lay, (int32_t)dc.B, dc.units);
   const int32_t B = (int32_t)dc.B, H = (int32_t)dc.H, L = (int32_t)dc.L, R = (int32_t)dc.R;
   MLA_TRY(cuda_status(launch_decode_schedule(seq_lens, B, max_blocks, dc.cv.page, s, st), "mla_decode schedule"));
@@ -294,6 +294,7 @@ mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, con
                                            descale_q, descale_k),
                         "mla_decode split kernel"));
   }
+  if (!combine) return MLA_OK;
   return cuda_status(launch_decode_combine(dtype, dc.ov, lse_out, seq_lens, B, H, L, s, st), "mla_decode combine");
 }
 
@@ -534,6 +535,80 @@ mla_status mla_decode_sparse_fp8(mla_dtype dtype, mla_tensor o_lat_out, float* l
                      "mla_decode_sparse_fp8 combine");
 }
 
+namespace {
+// mla_decode_v_up's workspace: mla_decode's layout, then o_lat [B, H, L] (4 bytes an element
+// covers both dtypes).
+struct VupWs {
+  DecodeWsLayout lay;
+  size_t off_olat, total;
+};
+VupWs vup_ws(int64_t B, int64_t H, int64_t L, int32_t units) {
+  VupWs w;
+  w.lay = decode_ws_layout(B, H, L, units);
+  w.off_olat = (w.lay.total + 255) & ~size_t(255);
+  w.total = (w.off_olat + (size_t)B * (size_t)H * (size_t)L * 4 + 255) & ~size_t(255);
+  return w;
+}
+}  // namespace
+
+size_t mla_decode_v_up_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank, int32_t num_splits) {
+  if (batch < 0 || num_heads < 0 || kv_lora_rank < 0 || num_splits < 0) return 0;
+  return vup_ws(batch, num_heads, kv_lora_rank, decode_units(num_splits)).total;
+}
+
+mla_status mla_decode_v_up(mla_dtype dtype, mla_tensor out, float* lse_out, mla_tensor q_cat, mla_tensor cache,
+                           const int32_t* block_table, int64_t block_table_stride, int32_t max_blocks,
+                           const int32_t* seq_lens, int32_t kv_lora_rank, int32_t rope_dim, float softmax_scale,
+                           mla_tensor w_uv, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat, 3, "q_cat"));
+  MLA_TRY(check_view(out, 3, "out"));
+  MLA_TRY(check_view(w_uv, 3, "w_uv"));
+  const int64_t B = q_cat.shape[0], H = q_cat.shape[1], L = kv_lora_rank, V = out.shape[2];
+  if (L <= 0 || rope_dim < 0) return fail(MLA_ERR_INVALID_ARG, "kv_lora_rank must be > 0 and rope_dim >= 0");
+  if (num_splits < 0) return fail(MLA_ERR_INVALID_ARG, "num_splits < 0");
+  if (out.shape[0] != B || out.shape[1] != H)
+    return fail(MLA_ERR_INVALID_ARG, "out must be [B,H,V] = [%lld,%lld,.]", (long long)B, (long long)H);
+  if (w_uv.shape[0] != H || w_uv.shape[1] != L || w_uv.shape[2] != V)
+    return fail(MLA_ERR_INVALID_ARG, "w_uv must be [H,L,V] = [%lld,%lld,%lld]", (long long)H, (long long)L,
+                (long long)V);
+  if (B == 0 || H == 0 || V == 0) return MLA_OK;
+  const VupWs ws = vup_ws(B, H, L, decode_units(num_splits));
+  if (workspace == nullptr || workspace_bytes < ws.total)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu bytes, need %zu", workspace_bytes, ws.total);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  // o_lat, the intermediate, lives in the workspace: [B, H, L] contiguous in dtype
+  mla_tensor o_lat{};
+  o_lat.data = static_cast<char*>(workspace) + ws.off_olat;
+  o_lat.rank = 3;
+  o_lat.shape[0] = B;
+  o_lat.shape[1] = H;
+  o_lat.shape[2] = L;
+  o_lat.stride[0] = H * L;
+  o_lat.stride[1] = L;
+  o_lat.stride[2] = 1;
+  DecodeCall dc;
+  MLA_TRY(check_decode_args(dtype, o_lat, q_cat, cache, block_table, block_table_stride, max_blocks, seq_lens,
+                            kv_lora_rank, rope_dim, softmax_scale, num_splits, &dc));
+  const cudaStream_t st = (cudaStream_t)stream;
+  MLA_TRY(run_decode(dtype, dc, lse_out, block_table, block_table_stride, max_blocks, seq_lens, softmax_scale,
+                     workspace, ws.lay, st, false, nullptr, nullptr, /*combine=*/false));
+  const DecodeSched s = decode_sched_from_ws(workspace, ws.lay, (int32_t)B, dc.units);
+  const View3 ov = view3(out), wv = view3(w_uv);
+  if (combine_vup_supported(dtype, (int)L, (int)V, ov, wv))
+    return cuda_status(launch_combine_vup(ov, dc.ov, lse_out, wv, (int32_t)B, (int32_t)H, (int32_t)V, s, st),
+                       "mla_decode_v_up combine + v_up");
+  // otherwise the two steps as separate kernels: the combine into o_lat, then the bmm
+  MLA_TRY(cuda_status(launch_decode_combine(dtype, dc.ov, lse_out, seq_lens, (int32_t)B, (int32_t)H, (int32_t)L, s, st),
+                      "mla_decode_v_up combine"));
+  const View3 out_hbv{out.data, H, B, V, out.stride[1], out.stride[0], out.stride[2]};
+  const View3 o_hbl{dc.ov.data, H, B, L, dc.ov.s1, dc.ov.s0, 1};
+  return cuda_status(launch_bmm(dtype, out_hbv, o_hbl, wv, st), "mla_decode_v_up v_up");
+}
+
 size_t mla_prefill_workspace_size(int32_t batch) {
   if (batch < 0) return 0;
   return ((size_t)(batch + 1) * sizeof(int32_t) + 255) & ~size_t(255);
@@ -598,7 +673,7 @@ mla_status mla_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "mla_device_error: stream synchronize");
   unsigned bits = copy_errors_read_clear() | attn_simt_errors_read_clear() | attn_tc_errors_read_clear() |
-                  bmm_tc_errors_read_clear();
+                  bmm_tc_errors_read_clear() | combine_vup_errors_read_clear();
   if (bits & kErrTimeout) return fail(MLA_ERR_TIMEOUT, "a bounded device-side wait gave up");
   if (bits & kErrDeviceData)
     return fail(MLA_ERR_DEVICE_DATA, "a slot, block id or sequence length was out of range");

@@ -142,6 +142,12 @@ cudaError_t launch_decode_sparse_simt(mla_dtype dt, const View3& o_lat, float* l
                                       const DsMlaCache& cache, const int32_t* indices, int64_t idx_stride,
                                       int32_t topk, int32_t B, int32_t H, float scale, const DecodeSched& s,
                                       cudaStream_t st);
+// The LSE combine and the W_UV un-projection in one kernel (combine_vup.cu): bf16, L = 512,
+// V a multiple of 128, v-contiguous out and W_UV views, W_UV 16-byte aligned.
+bool combine_vup_supported(mla_dtype dt, int L, int V, const View3& out, const View3& w_uv);
+// out[b, h, :] = combine(o_lat rows / partials of (b, h)) @ w_uv[h], o_lat rounded to bf16 first.
+cudaError_t launch_combine_vup(const View3& out, const View3& o_lat, float* lse, const View3& w_uv, int32_t B,
+                               int32_t H, int32_t V, const DecodeSched& s, cudaStream_t st);
 // The valid slots of each sparse query in listed order ([B, topk], compacted) and their counts.
 cudaError_t launch_sparse_compact(const int32_t* indices, int64_t idx_stride, int32_t topk, int32_t B,
                                   int64_t num_rows, int32_t* out, int32_t* counts, cudaStream_t st);
@@ -230,7 +236,7 @@ mla_status check_decode_args(mla_dtype dtype, const mla_tensor& o_lat_out, const
 mla_status run_decode(mla_dtype dtype, const DecodeCall& dc, float* lse_out, const int32_t* block_table,
                       int64_t block_table_stride, int32_t max_blocks, const int32_t* seq_lens, float softmax_scale,
                       void* scratch, const DecodeWsLayout& lay, cudaStream_t st, bool fp8_cache = false,
-                      const float* descale_q = nullptr, const float* descale_k = nullptr);
+                      const float* descale_q = nullptr, const float* descale_k = nullptr, bool combine = true);
 
 // Set (or clear, with MLA_OK) the calling thread's mla_last_error() message.
 mla_status report_status(mla_status st, const char* fmt, ...);
@@ -239,6 +245,7 @@ mla_status report_status(mla_status st, const char* fmt, ...);
 unsigned copy_errors_read_clear();
 unsigned attn_simt_errors_read_clear();
 unsigned attn_tc_errors_read_clear();
+unsigned combine_vup_errors_read_clear();
 unsigned bmm_tc_errors_read_clear();
 cudaError_t launch_wait_check(uint32_t limit_us, cudaStream_t st);
 

@@ -75,19 +75,27 @@ def test_clock_summary_takes_the_loaded_half_and_flags_throttle_reasons():
     assert s["reasons"] == ["sw_power_cap"]
 
 
-def test_traffic_record_is_used_only_for_the_source_it_was_taken_on(tmp_path, monkeypatch):
+def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
     csrc = tmp_path / "mla_latent_kv_11_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
-    src = b"// kernel source\n"
-    (csrc / "k.cu").write_bytes(src)
-    sha = hashlib.sha256(src).hexdigest()[:16]
+    (csrc / "k.cu").write_bytes(b"// kernel source\n")
+    (csrc / "c.cu").write_bytes(b"// combine source\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench._sources_sha(("k.cu", "c.cu"))
     (tmp_path / "profiles" / "traffic.json").write_text(
         json.dumps({"decode": {"source_sha": sha, "bytes_per_launch": 1234.0}}))
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench._traffic_for("k.cu") == 1234.0
-    (csrc / "k.cu").write_bytes(src + b"// changed\n")
-    assert bench._traffic_for("k.cu") is None
+    assert bench._traffic_for(("k.cu", "c.cu")) == 1234.0
+    (csrc / "c.cu").write_bytes(b"// combine source, changed\n")
+    assert bench._traffic_for(("k.cu", "c.cu")) is None
+    assert bench._traffic_for(("k.cu", "missing.cu")) is None
+
+
+def test_decode_v_up_counts_weights_and_out_instead_of_o_lat():
+    lens, B, H, L, R, V = [3, 70], 2, 4, 8, 2, 5
+    nbytes, flops = bench.decode_v_up_algorithmic(lens, B, H, L, R, V)
+    assert nbytes == bench.decode_algorithmic_bytes(lens, B, H, L, R, 0) - B * H * L * 2 + H * L * V * 2 + B * H * V * 2
+    assert flops == bench.decode_algorithmic_flops(lens, H, L, R) + 2 * B * H * L * V
 
 
 def test_reference_arm_prints_one_contract_line():

@@ -121,3 +121,64 @@ def test_prefill_pipeline_nope_sampled(mla):
                             (1, 0, 2))
     check_close(to_f64(o_lat)[rows], want_olat, dt, "prefill pipeline o_lat")
     check_close(to_f64(out)[rows], want_out, dt, "prefill pipeline out")
+
+
+def gpu_decode_v_up_step(mla, w, num_splits=0):
+    """Absorb, concat, cache write, then decode and v_up as the one call mla_decode_v_up;
+    returns (out, lse)."""
+    import torch
+    g, dt = w.geom, w.dtype
+    B, H, R, V, L = w.batch, g.n_head, g.d_rope, g.d_v, g.kv_rank
+    E = L + R
+    q_lat_store = poisoned((H, B, L), dt)
+    mla.mla_absorb_q(q_lat_store, to_dev(w.q_nope, dt).transpose(0, 1), to_dev(w.w_uk, dt))
+    q_cat = poisoned((B, H, E), dt)
+    mla.mla_concat_q(q_cat, q_lat_store.transpose(0, 1), to_dev(w.q_pe, dt))
+    cache = to_dev(w.full_cache(), dt)
+    mla.mla_cache_write(cache, to_dev(w.new_kv_c, dt), to_dev(w.new_k_pe, dt), torch.from_numpy(w.slots).cuda())
+    out = poisoned((B, H, V), dt)
+    lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
+    mla.mla_decode_v_up(out, q_cat, cache, torch.from_numpy(w.block_table).cuda(),
+                        torch.from_numpy(w.seq_lens).cuda(), L, R, w.scale, to_dev(w.w_uv, dt), lse_out=lse,
+                        num_splits=num_splits)
+    mla.mla_device_error()
+    return out, lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("splits", [0, 5])
+@pytest.mark.parametrize("which", ["v2lite_f32", "v3_bf16"])
+def test_decode_v_up_one_call_matches_oracle(mla, which, splits):
+    # bf16 at V = 128 runs the combine and the un-projection as one kernel; fp32 runs them as
+    # the separate kernels behind the same call
+    w = mi.v2_lite_decode() if which == "v2lite_f32" else mi.v3_decode_small()
+    out, lse = gpu_decode_v_up_step(mla, w, splits)
+    want_out, _, want_lse, _ = oracle_decode_step(w)
+    check_close(to_f64(out), want_out, w.dtype, f"{which} out, {splits} splits")
+    assert np.max(np.abs(lse - want_lse)) < (1e-3 if w.dtype == "f32" else 1.2e-2)
+
+
+def test_decode_v_up_equals_decode_then_v_up(mla):
+    # the fused kernel rounds o_lat to bf16 before the MMA as the two calls do; only the
+    # tensor core's summation order differs, so the outputs agree to about one bf16 step
+    w = mi.v3_decode_small()
+    out_sep, _, _ = gpu_decode_step(mla, w)
+    out_one, _ = gpu_decode_v_up_step(mla, w)
+    a, b = to_f64(out_sep), to_f64(out_one)
+    assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-6)
+
+
+def test_decode_v_up_nope_geometry_two_v_tiles_ragged_batch(mla):
+    # 64 heads, R = 0, V = 256 (two 128-wide v tiles), 70 sequences (two chunks of 64), ragged
+    # and empty lengths, split across units
+    lens = np.array([(37 * i * i + 11 * i) % 900 for i in range(70)], np.int32)
+    lens[5] = 0
+    lens[66] = 0
+    w = mi.decode_workload(mi.NOPE_64, "bf16", lens, 64, config_index=21, name="nope_vup")
+    out, lse = gpu_decode_v_up_step(mla, w, num_splits=40)
+    ids = [0, 5, 17, 33, 63, 64, 66, 69]
+    want_out, _, want_lse, _ = oracle_decode_step(w, ids)
+    check_close(to_f64(out)[ids], want_out, "bf16", "NoPE geometry out")
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(lse[ids]), fin)
+    assert np.max(np.abs(lse[ids][fin] - want_lse[fin])) < 1.2e-2
+    assert np.all(to_f64(out)[5] == 0) and np.all(to_f64(out)[66] == 0)
