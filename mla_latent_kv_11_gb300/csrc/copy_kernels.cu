@@ -43,6 +43,27 @@ __device__ __forceinline__ void row_lane(const RowSplit rs, int64_t& first_row, 
   c0 = lane & (rs.G - 1);
 }
 
+// One row: words [0, La) from a, [La, E) from b (b already offset by -La), lanes c0, c0 + G,
+// ... of a row group. A lane loads up to four words before it stores any, so a row costs one
+// memory latency instead of one per word.
+template <typename W>
+__device__ __forceinline__ void copy_row(W* __restrict__ o, const W* __restrict__ a, const W* __restrict__ b,
+                                         int La, int E, int c0, int G) {
+  for (int c = c0; c < E; c += 4 * G) {
+    W v[4] = {};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int cc = c + u * G;
+      if (cc < E) v[u] = cc < La ? a[cc] : b[cc];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int cc = c + u * G;
+      if (cc < E) o[cc] = v[u];
+    }
+  }
+}
+
 // q_cat[t,h,0:L] = nope[t,h,:]; q_cat[t,h,L:L+R] = rope[t,h,:] (rope s1 may be 0).
 // Counts and strides are in units of W (the copy word); L and R are multiples
 // of the word on the vector path. rows = T * H < 2^31.
@@ -61,7 +82,7 @@ __global__ void __launch_bounds__(256) concat_q_kernel(
     W* o = out + t * o_s0 + h * o_s1;
     const W* nr = nope + t * n_s0 + h * n_s1;
     const W* rr = rope + t * r_s0 + h * r_s1 - Lw;
-    for (int c = c0; c < Ew; c += rs.G) o[c] = c < Lw ? nr[c] : rr[c];
+    copy_row(o, nr, rr, Lw, Ew, c0, rs.G);
   }
 }
 
@@ -87,7 +108,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     W* o = cache + blk * c_blk + r * c_row;
     const W* kr = kv_c + tok * k_s0;
     const W* pr = k_pe + tok * p_s0 - Lw;
-    for (int c = c0; c < Ew; c += rs.G) o[c] = c < Lw ? kr[c] : pr[c];
+    copy_row(o, kr, pr, Lw, Ew, c0, rs.G);
   }
 }
 
@@ -219,7 +240,7 @@ __global__ void __launch_bounds__(256) concat_cache_kernel(ConcatArgs a, CacheAr
       uint4* o = a.out + t * a.o_s0 + h * a.o_s1;
       const uint4* nr = a.nope + t * a.n_s0 + h * a.n_s1;
       const uint4* rr = a.rope + t * a.r_s0 + h * a.r_s1 - a.Lw;
-      for (int cc = c0; cc < Ew; cc += rs.G) o[cc] = cc < a.Lw ? nr[cc] : rr[cc];
+      copy_row(o, nr, rr, a.Lw, Ew, c0, rs.G);
     }
   } else {
     const int Ew = c.Lw + c.Rw;
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(256) concat_cache_kernel(ConcatArgs a, CacheAr
       uint4* o = c.cache + blk * c.c_blk + row * c.c_row;
       const uint4* kr = c.kv_c + r * c.k_s0;
       const uint4* pr = c.k_pe + r * c.p_s0 - c.Lw;
-      for (int cc = c0; cc < Ew; cc += rs.G) o[cc] = cc < c.Lw ? kr[cc] : pr[cc];
+      copy_row(o, kr, pr, c.Lw, Ew, c0, rs.G);
     }
   }
 }
