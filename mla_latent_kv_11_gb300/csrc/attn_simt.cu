@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   __shared__ int warp_tot[32];
   __shared__ int carry_sh, starts_sh;
   __shared__ int pre_sh[kSchedSmemSeqs + 1], nz_sh[kSchedSmemSeqs + 1], ut_sh[kSchedSmemUnits + 1];
+  __shared__ int len_sh[kSchedSmemSeqs];   // clamped lengths, read from global memory once
   pdl_enter();
   const int W = s.units;
   const bool seqs_in_smem = B <= kSchedSmemSeqs, units_in_smem = W <= kSchedSmemUnits;
@@ -123,7 +124,9 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
   // pass 1: tile prefix
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    const int n = b < B ? (clamp_len(seq_lens, b, cap) + kTile - 1) / kTile : 0;
+    const int len = b < B ? clamp_len(seq_lens, b, cap) : 0;
+    if (seqs_in_smem && b < B) len_sh[b] = len;
+    const int n = (len + kTile - 1) / kTile;
     int tot;
     const int ex = block_exclusive_scan(n, warp_tot, &tot);
     const int carry = carry_sh;
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t* __
     if (b < B) {
       s.piece_base[b] = carry + ex;
       // everything a tensor-core walker needs about b in one 16-byte load
-      const int len = seq_lens == nullptr ? cap : min(max(seq_lens[b], 0), cap);
+      const int len = seqs_in_smem ? len_sh[b] : (seq_lens == nullptr ? cap : min(max(seq_lens[b], 0), cap));
       s.seqinfo[b] = make_int4(pre[b], len, np, carry + ex - fu);
     }
     __syncthreads();
