@@ -302,41 +302,50 @@ __device__ __forceinline__ float exp2_int(float d) {
   return d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
 }
 
-// Four e4m3 codes (one word, low byte first) -> their values as fp32. A code's exponent and
-// mantissa bits placed in an fp32's exponent and mantissa fields read as value * 2^-120 (an fp32
-// subnormal for exponent 0, which the multiply honours), so one multiply by 2^120 gives every
-// finite value exactly; the sign bit goes to bit 31 first. `mul` may carry a further factor.
-__device__ __forceinline__ void e4m3x4_values(uint32_t x, float mul, float (&f)[4]) {
-  f[0] = __uint_as_float(((x << 24) & 0x80000000u) | ((x << 20) & 0x07F00000u)) * 0x1p120f * mul;
-  f[1] = __uint_as_float(((x << 16) & 0x80000000u) | ((x << 12) & 0x07F00000u)) * 0x1p120f * mul;
-  f[2] = __uint_as_float(((x << 8) & 0x80000000u) | ((x << 4) & 0x07F00000u)) * 0x1p120f * mul;
-  f[3] = __uint_as_float((x & 0x80000000u) | ((x >> 4) & 0x07F00000u)) * 0x1p120f * mul;
-  // the two NaN codes (all exponent and mantissa bits set) are rare: patched here
-  if ((((x & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (((x >> (8 * k)) & 0x7Fu) == 0x7Fu) f[k] = __uint_as_float(0x7FC00000u);
-  }
+// e4m3 -> bf16 in shared memory. A code's exponent and mantissa bits placed in an fp32's
+// exponent and mantissa fields read as value * 2^-120 (an fp32 subnormal for exponent 0, which
+// the multiply honours), so one multiply by 2^120 gives every finite value exactly; the sign
+// bit goes to bit 31 first. Byte k of the word x is code k.
+__device__ __forceinline__ float e4m3_at(uint32_t x, int k, float mul) {
+  return __uint_as_float(((x << (24 - 8 * k)) & 0x80000000u) | (((x >> (8 * k)) << 20) & 0x07F00000u)) *
+         0x1p120f * mul;
 }
 
-// 16 codes -> 16 bf16 (eight words, low value first): exact (truncating an fp32 that holds an
-// e4m3 value exactly), or with a scale each product rounded to nearest.
+// The two NaN codes (every exponent and mantissa bit set) would read as +-480: their bf16
+// halves are replaced by NaN, without a branch. `sel` picks the two bytes of x that the packed
+// word holds (0x9988: bytes 0 and 1, 0xBBAA: bytes 2 and 3; the permute replicates each
+// byte's top bit over 8 bits).
+__device__ __forceinline__ uint32_t nan_patch(uint32_t packed, uint32_t x, uint32_t sel) {
+  const uint32_t nan_bytes = ((x & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;   // bit 7: code is NaN
+  const uint32_t mask = __byte_perm(nan_bytes, 0u, sel);
+  return (packed & ~mask) | (0x7FC07FC0u & mask);
+}
+
+// Four codes -> two words of two bf16 each (low value first): exact (an fp32 holding an e4m3
+// value truncates to bf16 exactly), or with a scale each product rounded to nearest.
 template <bool kScaled>
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 w, float sc, uint32_t (&o)[8]) {
-  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float f[4];
-    e4m3x4_values(wv[k], kScaled ? sc : 1.f, f);
-    if (kScaled) {
-      const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
-      o[2 * k] = *reinterpret_cast<const uint32_t*>(&a);
-      o[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b);
-    } else {
-      o[2 * k] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632);
-      o[2 * k + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632);
-    }
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t x, float sc, uint32_t& lo, uint32_t& hi) {
+  const float f0 = e4m3_at(x, 0, kScaled ? sc : 1.f), f1 = e4m3_at(x, 1, kScaled ? sc : 1.f);
+  const float f2 = e4m3_at(x, 2, kScaled ? sc : 1.f), f3 = e4m3_at(x, 3, kScaled ? sc : 1.f);
+  if (kScaled) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
+    lo = *reinterpret_cast<const uint32_t*>(&a);
+    hi = *reinterpret_cast<const uint32_t*>(&b);
+  } else {
+    lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+    hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
   }
+  lo = nan_patch(lo, x, 0x9988u);
+  hi = nan_patch(hi, x, 0xBBAAu);
+}
+
+// 16 codes (one 16-byte granule) -> 16 bf16 as two 16-byte chunks.
+template <bool kScaled>
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 w, float sc, uint4& c0, uint4& c1) {
+  e4m3x4_to_bf16<kScaled>(w.x, sc, c0.x, c0.y);
+  e4m3x4_to_bf16<kScaled>(w.y, sc, c0.z, c0.w);
+  e4m3x4_to_bf16<kScaled>(w.z, sc, c1.x, c1.y);
+  e4m3x4_to_bf16<kScaled>(w.w, sc, c1.z, c1.w);
 }
 
 __device__ __forceinline__ int ntiles(const Seg& s) { return (s.k1 - s.k0 + kKeysT - 1) / kKeysT; }
@@ -596,24 +605,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (g < 16) {
             // 16 latent codes -> 16 bf16: two 16-byte chunks of box g / 4
             const uint4 w = *reinterpret_cast<const uint4*>(row + g * 16);
-            uint32_t o[8];
+            uint4 c0, c1;
             if (kSrc == 1)
-              e4m3x16_to_bf16<false>(w, 1.f, o);
+              e4m3x16_to_bf16<false>(w, 1.f, c0, c1);
             else
-              e4m3x16_to_bf16<true>(w, reinterpret_cast<const float*>(row + 16 * 16)[2 * (int)rank + g / 8], o);
+              e4m3x16_to_bf16<true>(w, reinterpret_cast<const float*>(row + 16 * 16)[2 * (int)rank + g / 8], c0, c1);
             unsigned char* bx = dst + (g >> 2) * kBoxBytesK + r * 128;
             const int j0 = (g & 3) * 2;
-            *reinterpret_cast<uint4*>(bx + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(bx + ((j0 ^ (r & 7)) << 4)) = c0;
+            *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ (r & 7)) << 4)) = c1;
           } else {
             // rope: 64-byte rows of the rope box, 64-byte swizzle
             unsigned char* bx = dst + 4 * kBoxBytesK + r * 64;
             if (kSrc == 1) {
-              uint32_t o[8];
-              e4m3x16_to_bf16<false>(*reinterpret_cast<const uint4*>(row + g * 16), 1.f, o);
+              uint4 c0, c1;
+              e4m3x16_to_bf16<false>(*reinterpret_cast<const uint4*>(row + g * 16), 1.f, c0, c1);
               const int j0 = (g - 16) * 2;
-              *reinterpret_cast<uint4*>(bx + ((j0 ^ ((r >> 1) & 3)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ ((r >> 1) & 3)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+              *reinterpret_cast<uint4*>(bx + ((j0 ^ ((r >> 1) & 3)) << 4)) = c0;
+              *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ ((r >> 1) & 3)) << 4)) = c1;
             } else {
               const int jr = g - 16;   // bf16 already: one chunk, from staged granule 17 + jr
               *reinterpret_cast<uint4*>(bx + ((jr ^ ((r >> 1) & 3)) << 4)) =
