@@ -522,7 +522,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // tile to bf16 in the swizzled layout of a TMA box once its bf16 stage is free
       const int lt = (warp == 0 ? 0 : 32) + lane;
       constexpr int G = C::kGran;
-      constexpr int GC = kSrc == 1 ? G : 20;     // granules converted per row (the scales are read)
       auto group_all = [](bool v) { return named_bar_and(kLoadBar, kLoaders, v); };
       int64_t* rowbase = reinterpret_cast<int64_t*>(smem + C::kOffRowBase);
       unsigned char* stg = smem + C::kOffStg;
@@ -572,15 +571,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           named_bar(kLoadBar, kLoaders);
           MLA_TRACE3_AT(1, gi);
           const uint32_t dst0 = smem_u32(stg + u * C::kStgBytes);
-          for (int f = lt; f < kKeysT * G; f += kLoaders) {
-            const int r = f / G, g = f - r * G;
+          // the 16 latent granules of every row, then the tail granules (rope; and the scales
+          // of a ds_mla entry): one loop each, so no lane of a warp takes the other kind
+#pragma unroll 4
+          for (int f = lt; f < kKeysT * 16; f += kLoaders) {
+            const int r = f >> 4, g = f & 15;
             const int64_t off = rb[r];
-            int byte;
-            if (kSrc == 1)
-              byte = g < 16 ? col0 + 16 * g : 512 + kRopeHalf * (int)rank + 16 * (g - 16);
-            else
-              byte = g < 16 ? col0 + 16 * g : g == 16 ? kDsMlaLatent : kDsMlaRopeByte + 64 * (int)rank + 16 * (g - 17);
-            cp_async16(dst0 + f * 16, p.cache8 + (off < 0 ? 0 : off + byte), off < 0 ? 0u : 16u);
+            cp_async16(dst0 + (r * G + g) * 16, p.cache8 + (off < 0 ? 0 : off + col0 + 16 * g), off < 0 ? 0u : 16u);
+          }
+          constexpr int TG = G > 16 ? G - 16 : 1;   // tail granules per row (none without rope)
+          for (int f = lt; f < kKeysT * (G - 16); f += kLoaders) {
+            const int r = f / TG, g = f - r * TG;
+            const int64_t off = rb[r];
+            const int byte = kSrc == 1 ? 512 + kRopeHalf * (int)rank + 16 * g
+                                       : (g == 0 ? kDsMlaLatent : kDsMlaRopeByte + 64 * (int)rank + 16 * (g - 1));
+            cp_async16(dst0 + (r * G + 16 + g) * 16, p.cache8 + (off < 0 ? 0 : off + byte), off < 0 ? 0u : 16u);
           }
           cp_async_commit();
           cp_async_arrive_noinc(&bars.stg_full[u]);
@@ -599,34 +604,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const unsigned char* src = stg + u * C::kStgBytes;
         unsigned char* dst = sKV + s * C::kStageBytes;
-        for (int f = lt; f < kKeysT * GC; f += kLoaders) {
-          const int r = f / GC, g = f - r * GC;
+        // latent: 16 codes per staged granule -> 16 bf16, two 16-byte chunks of box g / 4 (one
+        // loop per part, so the lanes of a warp never split between the two)
+#pragma unroll 2
+        for (int f = lt; f < kKeysT * 16; f += kLoaders) {
+          const int r = f >> 4, g = f & 15;
           const unsigned char* row = src + r * G * 16;
-          if (g < 16) {
-            // 16 latent codes -> 16 bf16: two 16-byte chunks of box g / 4
-            const uint4 w = *reinterpret_cast<const uint4*>(row + g * 16);
-            uint4 c0, c1;
-            if (kSrc == 1)
-              e4m3x16_to_bf16<false>(w, 1.f, c0, c1);
-            else
-              e4m3x16_to_bf16<true>(w, reinterpret_cast<const float*>(row + 16 * 16)[2 * (int)rank + g / 8], c0, c1);
-            unsigned char* bx = dst + (g >> 2) * kBoxBytesK + r * 128;
-            const int j0 = (g & 3) * 2;
-            *reinterpret_cast<uint4*>(bx + ((j0 ^ (r & 7)) << 4)) = c0;
-            *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ (r & 7)) << 4)) = c1;
-          } else {
-            // rope: 64-byte rows of the rope box, 64-byte swizzle
+          const uint4 w = *reinterpret_cast<const uint4*>(row + g * 16);
+          uint4 c0, c1;
+          if (kSrc == 1)
+            e4m3x16_to_bf16<false>(w, 1.f, c0, c1);
+          else
+            e4m3x16_to_bf16<true>(w, reinterpret_cast<const float*>(row + 16 * 16)[2 * (int)rank + g / 8], c0, c1);
+          unsigned char* bx = dst + (g >> 2) * kBoxBytesK + r * 128;
+          const int j0 = (g & 3) * 2;
+          *reinterpret_cast<uint4*>(bx + ((j0 ^ (r & 7)) << 4)) = c0;
+          *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ (r & 7)) << 4)) = c1;
+        }
+        // rope: 64-byte rows of the rope box, 64-byte swizzle
+        if (kRope) {
+          constexpr int RG = kSrc == 1 ? 2 : 4;   // staged rope granules per row
+          for (int f = lt; f < kKeysT * RG; f += kLoaders) {
+            const int r = f / RG, g = f - r * RG;
+            const unsigned char* row = src + r * G * 16;
             unsigned char* bx = dst + 4 * kBoxBytesK + r * 64;
             if (kSrc == 1) {
               uint4 c0, c1;
-              e4m3x16_to_bf16<false>(*reinterpret_cast<const uint4*>(row + g * 16), 1.f, c0, c1);
-              const int j0 = (g - 16) * 2;
+              e4m3x16_to_bf16<false>(*reinterpret_cast<const uint4*>(row + (16 + g) * 16), 1.f, c0, c1);
+              const int j0 = g * 2;
               *reinterpret_cast<uint4*>(bx + ((j0 ^ ((r >> 1) & 3)) << 4)) = c0;
               *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ ((r >> 1) & 3)) << 4)) = c1;
             } else {
-              const int jr = g - 16;   // bf16 already: one chunk, from staged granule 17 + jr
-              *reinterpret_cast<uint4*>(bx + ((jr ^ ((r >> 1) & 3)) << 4)) =
-                  *reinterpret_cast<const uint4*>(row + (17 + jr) * 16);
+              // bf16 already: one chunk, from staged granule 17 + g (16 holds the scales)
+              *reinterpret_cast<uint4*>(bx + ((g ^ ((r >> 1) & 3)) << 4)) =
+                  *reinterpret_cast<const uint4*>(row + (17 + g) * 16);
             }
           }
         }
