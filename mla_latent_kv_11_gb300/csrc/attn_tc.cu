@@ -223,6 +223,7 @@ struct TcParams {
   const float* descale_k;
   const int32_t* slots;
   int64_t slot_stride;
+  int fp8_tma;       // kSrc 1: whole pages of rows come as TMA boxes (else per-row gathers)
   // prefill
   const int32_t* cu_q;
   const int32_t* kv_lens;
@@ -321,19 +322,27 @@ __device__ __forceinline__ uint32_t nan_patch(uint32_t packed, uint32_t x, uint3
   return (packed & ~mask) | (0x7FC07FC0u & mask);
 }
 
-// Four codes -> two words of two bf16 each (low value first): exact (an fp32 holding an e4m3
-// value truncates to bf16 exactly), or with a scale each product rounded to nearest.
+// Two codes (bytes b0 and b1 of x, selected by `spread`) -> a bf16x2 word, exactly: the same
+// bit placement in bf16 lanes (value * 2^-120, a bf16 subnormal for exponent 0) times 2^120.
+__device__ __forceinline__ uint32_t e4m3x2_bf16(uint32_t x, uint32_t spread) {
+  const uint32_t t = __byte_perm(x, 0u, spread);   // code k in bits [16k, 16k + 8)
+  const uint32_t bits = ((t << 4) & 0x07F007F0u) | ((t << 8) & 0x80008000u);
+  const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&bits), __float2bfloat162_rn(0x1p120f));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Four codes -> two words of two bf16 each (low value first): exact, or with a scale each
+// product rounded to nearest.
 template <bool kScaled>
 __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t x, float sc, uint32_t& lo, uint32_t& hi) {
-  const float f0 = e4m3_at(x, 0, kScaled ? sc : 1.f), f1 = e4m3_at(x, 1, kScaled ? sc : 1.f);
-  const float f2 = e4m3_at(x, 2, kScaled ? sc : 1.f), f3 = e4m3_at(x, 3, kScaled ? sc : 1.f);
   if (kScaled) {
+    const float f0 = e4m3_at(x, 0, sc), f1 = e4m3_at(x, 1, sc), f2 = e4m3_at(x, 2, sc), f3 = e4m3_at(x, 3, sc);
     const __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
     lo = *reinterpret_cast<const uint32_t*>(&a);
     hi = *reinterpret_cast<const uint32_t*>(&b);
   } else {
-    lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-    hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+    lo = e4m3x2_bf16(x, 0x4140u);   // bytes 0 and 1
+    hi = e4m3x2_bf16(x, 0x4342u);   // bytes 2 and 3
   }
   lo = nan_patch(lo, x, 0x9988u);
   hi = nan_patch(hi, x, 0xBBAAu);
@@ -387,7 +396,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bars.kv_empty[s], 1);
     }
     for (int u = 0; u < C::kStg; ++u) {
-      mbar_init(&bars.stg_full[u], kLoaders);
+      // TMA boxes: one expect-tx arrival; gathers: one cp.async arrival per loader thread
+      mbar_init(&bars.stg_full[u], (kSrc == 1 && p.fp8_tma) ? 1 : kLoaders);
       mbar_init(&bars.stg_empty[u], kLoaders);
     }
     mbar_init(&bars.s_full, 1);
@@ -531,7 +541,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int nt = 0, j = 0;           // tiles of the current segment, next tile in it
       bool have = false;           // a segment is open
       int gi = 0, gc = 0;          // tiles issued, tiles converted
-      bool ok = true, more = true;
+      int blk_pf = -1, blk_now = -1;   // block ids of the next 32 tiles (a lane each) and of this one
+      bool ok = true, more = true;     // ok: the group's decision, the same in every loader thread
+      bool iss_ok = true;              // the issuing thread's own waits (TMA'd pages)
       while (ok) {
         // ---- issue: up to kStg tiles ahead of the conversion
         while (ok && more && gi < gc + C::kStg) {
@@ -547,48 +559,100 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!more) break;
           const int u = gi % C::kStg;
           MLA_TRACE3_AT(0, gi);
-          ok = group_all(mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort));
-          if (!ok) break;
-          // byte offset of each row of the tile (-1: past the segment or a bad block id)
-          int64_t* rb = rowbase + (gi & 1) * kKeysT;
-          {
-            const int t = sg.k0 + j * kKeysT + lt;
-            int64_t off = -1;
-            if (t < sg.k1) {
-              if (kSrc == 1) {
-                const int blk = p.block_table[(int64_t)sg.b * p.bt_stride + t / p.page];
-                if (blk >= 0 && blk < p.num_blocks)
-                  off = (int64_t)blk * p.s_blk8 + (int64_t)(t % p.page) * p.s_row8;
-                else
-                  atomicOr(&g_tc_err, kErrDeviceData);
-              } else {
-                const int slot = p.slots[(int64_t)sg.b * p.slot_stride + t];   // compacted: in range
-                off = (int64_t)(slot / p.page) * p.s_blk8 + (int64_t)(slot % p.page) * p.s_row8;
+          if (kSrc == 1 && p.fp8_tma) {
+            // whole pages of rows: one thread issues this CTA's latent box (and rope box) of every
+            // page the tile spans; rows past the segment and rows of a page that could not load
+            // are zeroed by the conversion (the slot's metadata says which). With pages of 64 rows
+            // or more, the lanes of warp 0 fetch the block ids of the next 32 tiles of the
+            // segment at once. The other loader threads do not wait here: a failed wait reaches
+            // them through the next group decision (the conversion's).
+            const int rows_box = min(p.page, kKeysT), subs = kKeysT / rows_box;
+            const int kt = sg.k0 + j * kKeysT;
+            if (subs == 1 && warp == 0) {
+              if ((j & 31) == 0) {
+                const int jj = j + lane;
+                blk_pf = jj < nt ? p.block_table[(int64_t)sg.b * p.bt_stride + (sg.k0 + jj * kKeysT) / p.page] : -1;
+              }
+              blk_now = __shfl_sync(0xffffffffu, blk_pf, j & 31);
+            }
+            if (lt == 0 && iss_ok) {
+              iss_ok = mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort);
+              if (iss_ok) {
+                int blks[8];
+                uint32_t bytes = 0;
+                int bad = 0;
+                for (int i = 0; i < subs; ++i) {
+                  const int key = kt + i * rows_box;
+                  blks[i] = -1;
+                  if (key >= sg.k1) continue;
+                  const int blk = subs == 1 ? blk_now : p.block_table[(int64_t)sg.b * p.bt_stride + key / p.page];
+                  if (blk < 0 || blk >= p.num_blocks) {
+                    atomicOr(&g_tc_err, kErrDeviceData);
+                    bad |= 1 << i;
+                    continue;
+                  }
+                  blks[i] = blk;
+                  bytes += (uint32_t)(rows_box * (256 + (kRope ? kRopeHalf : 0)));
+                }
+                int* meta = reinterpret_cast<int*>(smem + C::kOffRowBase);
+                meta[2 * u] = min(kKeysT, sg.k1 - kt);   // rows kept
+                meta[2 * u + 1] = bad;                   // bit i: page i of the tile did not load
+                mbar_arrive_expect_tx(&bars.stg_full[u], bytes);
+                unsigned char* dst = stg + u * C::kStgBytes;
+                const int row0 = subs == 1 ? kt % p.page : 0;
+                for (int i = 0; i < subs; ++i) {
+                  if (blks[i] < 0) continue;
+                  tma_load_3d(dst + i * rows_box * 256, &kvmap, &bars.stg_full[u], col0, row0, blks[i]);
+                  if (kRope)
+                    tma_load_3d(dst + kKeysT * 256 + i * rows_box * kRopeHalf, &ropemap, &bars.stg_full[u],
+                                512 + kRopeHalf * (int)rank, row0, blks[i]);
+                }
               }
             }
-            rb[lt] = off;
+          } else {
+            ok = group_all(mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort));
+            if (!ok) break;
+            // byte offset of each row of the tile (-1: past the segment or a bad block id)
+            int64_t* rb = rowbase + (gi & 1) * kKeysT;
+            {
+              const int t = sg.k0 + j * kKeysT + lt;
+              int64_t off = -1;
+              if (t < sg.k1) {
+                if (kSrc == 1) {
+                  const int blk = p.block_table[(int64_t)sg.b * p.bt_stride + t / p.page];
+                  if (blk >= 0 && blk < p.num_blocks)
+                    off = (int64_t)blk * p.s_blk8 + (int64_t)(t % p.page) * p.s_row8;
+                  else
+                    atomicOr(&g_tc_err, kErrDeviceData);
+                } else {
+                  const int slot = p.slots[(int64_t)sg.b * p.slot_stride + t];   // compacted: in range
+                  off = (int64_t)(slot / p.page) * p.s_blk8 + (int64_t)(slot % p.page) * p.s_row8;
+                }
+              }
+              rb[lt] = off;
+            }
+            named_bar(kLoadBar, kLoaders);
+            MLA_TRACE3_AT(1, gi);
+            const uint32_t dst0 = smem_u32(stg + u * C::kStgBytes);
+            // the 16 latent granules of every row, then the tail granules (rope; and the scales
+            // of a ds_mla entry): one loop each, so no lane of a warp takes the other kind
+  #pragma unroll 4
+            for (int f = lt; f < kKeysT * 16; f += kLoaders) {
+              const int r = f >> 4, g = f & 15;
+              const int64_t off = rb[r];
+              cp_async16(dst0 + (r * G + g) * 16, p.cache8 + (off < 0 ? 0 : off + col0 + 16 * g), off < 0 ? 0u : 16u);
+            }
+            constexpr int TG = G > 16 ? G - 16 : 1;   // tail granules per row (none without rope)
+            for (int f = lt; f < kKeysT * (G - 16); f += kLoaders) {
+              const int r = f / TG, g = f - r * TG;
+              const int64_t off = rb[r];
+              const int byte = kSrc == 1 ? 512 + kRopeHalf * (int)rank + 16 * g
+                                         : (g == 0 ? kDsMlaLatent : kDsMlaRopeByte + 64 * (int)rank + 16 * (g - 1));
+              cp_async16(dst0 + (r * G + 16 + g) * 16, p.cache8 + (off < 0 ? 0 : off + byte), off < 0 ? 0u : 16u);
+            }
+            cp_async_commit();
+            cp_async_arrive_noinc(&bars.stg_full[u]);
           }
-          named_bar(kLoadBar, kLoaders);
-          MLA_TRACE3_AT(1, gi);
-          const uint32_t dst0 = smem_u32(stg + u * C::kStgBytes);
-          // the 16 latent granules of every row, then the tail granules (rope; and the scales
-          // of a ds_mla entry): one loop each, so no lane of a warp takes the other kind
-#pragma unroll 4
-          for (int f = lt; f < kKeysT * 16; f += kLoaders) {
-            const int r = f >> 4, g = f & 15;
-            const int64_t off = rb[r];
-            cp_async16(dst0 + (r * G + g) * 16, p.cache8 + (off < 0 ? 0 : off + col0 + 16 * g), off < 0 ? 0u : 16u);
-          }
-          constexpr int TG = G > 16 ? G - 16 : 1;   // tail granules per row (none without rope)
-          for (int f = lt; f < kKeysT * (G - 16); f += kLoaders) {
-            const int r = f / TG, g = f - r * TG;
-            const int64_t off = rb[r];
-            const int byte = kSrc == 1 ? 512 + kRopeHalf * (int)rank + 16 * g
-                                       : (g == 0 ? kDsMlaLatent : kDsMlaRopeByte + 64 * (int)rank + 16 * (g - 1));
-            cp_async16(dst0 + (r * G + 16 + g) * 16, p.cache8 + (off < 0 ? 0 : off + byte), off < 0 ? 0u : 16u);
-          }
-          cp_async_commit();
-          cp_async_arrive_noinc(&bars.stg_full[u]);
           MLA_TRACE3_AT(2, gi);
           ++gi;
           ++j;
@@ -597,20 +661,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- convert tile gc: staging slot u -> bf16 stage s
         const int u = gc % C::kStg, s = gc % C::kStages;
         MLA_TRACE3_AT(3, gc);
-        ok = mbar_wait(&bars.stg_full[u], (gc / C::kStg) & 1, abort);
+        bool mine = iss_ok && mbar_wait(&bars.stg_full[u], (gc / C::kStg) & 1, abort);
         MLA_TRACE3_AT(4, gc);
-        ok = group_all(ok && mbar_wait(&bars.kv_empty[s], ((gc / C::kStages) & 1) ^ 1, abort));
+        ok = group_all(mine && mbar_wait(&bars.kv_empty[s], ((gc / C::kStages) & 1) ^ 1, abort));
         MLA_TRACE3_AT(5, gc);
         if (!ok) break;
         const unsigned char* src = stg + u * C::kStgBytes;
         unsigned char* dst = sKV + s * C::kStageBytes;
+        // TMA'd pages sit as [64 rows x 256 B] latent then [64 rows x 32 B] rope; gathered rows as
+        // rows of G granules. Rows at or past `keep` and rows of pages in `bad` are zeroed.
+        const bool boxes = kSrc == 1 && p.fp8_tma;
+        int keep = kKeysT, bad = 0, box_shift = 6;
+        if (boxes) {
+          const int* meta = reinterpret_cast<const int*>(smem + C::kOffRowBase);
+          keep = meta[2 * u];
+          bad = meta[2 * u + 1];
+          box_shift = 31 - __clz(min(p.page, kKeysT));
+        }
+        auto dropped = [&](int r) { return r >= keep || ((bad >> (r >> box_shift)) & 1); };
         // latent: 16 codes per staged granule -> 16 bf16, two 16-byte chunks of box g / 4 (one
         // loop per part, so the lanes of a warp never split between the two)
 #pragma unroll 2
         for (int f = lt; f < kKeysT * 16; f += kLoaders) {
           const int r = f >> 4, g = f & 15;
           const unsigned char* row = src + r * G * 16;
-          const uint4 w = *reinterpret_cast<const uint4*>(row + g * 16);
+          uint4 w = *reinterpret_cast<const uint4*>(boxes ? src + r * 256 + g * 16 : row + g * 16);
+          if (boxes && dropped(r)) w = make_uint4(0u, 0u, 0u, 0u);
           uint4 c0, c1;
           if (kSrc == 1)
             e4m3x16_to_bf16<false>(w, 1.f, c0, c1);
@@ -629,8 +705,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const unsigned char* row = src + r * G * 16;
             unsigned char* bx = dst + 4 * kBoxBytesK + r * 64;
             if (kSrc == 1) {
+              uint4 w = *reinterpret_cast<const uint4*>(boxes ? src + kKeysT * 256 + r * 32 + g * 16
+                                                              : row + (16 + g) * 16);
+              if (boxes && dropped(r)) w = make_uint4(0u, 0u, 0u, 0u);
               uint4 c0, c1;
-              e4m3x16_to_bf16<false>(*reinterpret_cast<const uint4*>(row + (16 + g) * 16), 1.f, c0, c1);
+              e4m3x16_to_bf16<false>(w, 1.f, c0, c1);
               const int j0 = g * 2;
               *reinterpret_cast<uint4*>(bx + ((j0 ^ ((r >> 1) & 3)) << 4)) = c0;
               *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ ((r >> 1) & 3)) << 4)) = c1;
@@ -1269,14 +1348,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool tensor_maps_available() { return encode_fn() != nullptr; }
 
 bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
-                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz) {
+                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz,
+                CUtensorMapDataType dt) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {s1_bytes, s2_bytes};
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1398,9 +1478,23 @@ cudaError_t launch_decode_tc_fp8(const View3& o_lat, float* lse, const View3& q,
   p.s_row8 = cache.s_row;
   p.descale_q = descale_q;
   p.descale_k = descale_k;
-  CUtensorMap none{};
-  if (R == 0) return launch_tc<0, 1>(p, none, none, s.units, st);
-  return launch_tc<64, 1>(p, none, none, s.units, st);
+  // pages of whole 64-row tiles (or tiles of whole pages) come as TMA boxes of bytes: this CTA's
+  // 256 latent codes and 32 rope codes of every row; other page sizes are gathered row by row
+  CUtensorMap km{}, rm{};
+  const int page = cache.page;
+  const uint32_t rows_box = page < 64 ? (uint32_t)page : 64u;
+  const uint64_t E = 512 + (uint64_t)R;
+  p.fp8_tma = (page % 64 == 0 || (64 % page == 0 && page % 8 == 0)) &&
+              make_map3d(&km, cache.data, E, (uint64_t)page, (uint64_t)cache.num_blocks, (uint64_t)cache.s_row,
+                         (uint64_t)cache.s_blk, 256, rows_box, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_DATA_TYPE_UINT8) &&
+              (R == 0 || make_map3d(&rm, cache.data, E, (uint64_t)page, (uint64_t)cache.num_blocks,
+                                    (uint64_t)cache.s_row, (uint64_t)cache.s_blk, kRopeHalf, rows_box, 1,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+                  ? 1
+                  : 0;
+  if (R == 0) return launch_tc<0, 1>(p, km, km, s.units, st);
+  return launch_tc<64, 1>(p, km, rm, s.units, st);
 }
 
 cudaError_t launch_decode_tc_dsmla(const View3& o_lat, float* lse, const View3& q, const DsMlaCache& cache,

@@ -108,9 +108,11 @@ DecodeSched decode_sched_from_ws(void* ws, const DecodeWsLayout& lay, int32_t B,
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
-// A 3-D bf16 TMA map (dims innermost first, strides of dims 1 and 2 in bytes, box b0 x b1 x b2).
+// A 3-D TMA map (dims innermost first, strides of dims 1 and 2 in bytes, box b0 x b1 x b2) of
+// bf16 elements, or of another element type.
 bool make_map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
-                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz);
+                uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz,
+                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 // True once the driver's tensor-map encoder has been found.
 bool tensor_maps_available();
 

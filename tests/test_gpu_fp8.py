@@ -153,8 +153,10 @@ def test_fp8_write_then_decode_round_trip(mla):
 
 
 @pytest.mark.parametrize("H,R,page,dq,dk", [(128, 64, 16, -0.5, 2.0), (64, 0, 128, 1.0, 0.25),
-                                           (64, 64, 64, 2.0, -1.0), (128, 0, 64, 1.0, 1.0)],
-                         ids=["h128_page16_neg_dq", "h64_nope_page128", "h64_rope_neg_dk", "h128_nope"])
+                                           (64, 64, 64, 2.0, -1.0), (128, 0, 64, 1.0, 1.0),
+                                           (128, 64, 48, 1.0, 0.5)],
+                         ids=["h128_page16_neg_dq", "h64_nope_page128", "h64_rope_neg_dk", "h128_nope",
+                              "h128_page48_rows_gathered"])
 def test_fp8_decode_bf16_queries_geometries_and_descale_signs(mla, H, R, page, dq, dk):
     # the bf16-query decode over e4m3 rows at other head counts, rope widths and page sizes, with
     # descales of either sign (the score scale is then negative: the row maximum must follow)
