@@ -313,12 +313,11 @@ __device__ __forceinline__ float e4m3_at(uint32_t x, int k, float mul) {
 }
 
 // The two NaN codes (every exponent and mantissa bit set) would read as +-480: their bf16
-// halves are replaced by NaN, without a branch. `sel` picks the two bytes of x that the packed
-// word holds (0x9988: bytes 0 and 1, 0xBBAA: bytes 2 and 3; the permute replicates each
-// byte's top bit over 8 bits).
+// halves are replaced by NaN. `sel` picks the two bytes of x that the packed word holds
+// (0x1100: bytes 0 and 1, 0x3322: bytes 2 and 3), each widened to its 16-bit half.
 __device__ __forceinline__ uint32_t nan_patch(uint32_t packed, uint32_t x, uint32_t sel) {
-  const uint32_t nan_bytes = ((x & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;   // bit 7: code is NaN
-  const uint32_t mask = __byte_perm(nan_bytes, 0u, sel);
+  const uint32_t nan = ((x & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;   // bit 7: code is NaN
+  const uint32_t mask = __byte_perm((nan >> 7) * 0xFFu, 0u, sel);          // 0xFF per NaN byte
   return (packed & ~mask) | (0x7FC07FC0u & mask);
 }
 
@@ -344,17 +343,24 @@ __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t x, float sc, uint32_t& l
     lo = e4m3x2_bf16(x, 0x4140u);   // bytes 0 and 1
     hi = e4m3x2_bf16(x, 0x4342u);   // bytes 2 and 3
   }
-  lo = nan_patch(lo, x, 0x9988u);
-  hi = nan_patch(hi, x, 0xBBAAu);
 }
 
-// 16 codes (one 16-byte granule) -> 16 bf16 as two 16-byte chunks.
+// 16 codes (one 16-byte granule) -> 16 bf16 as two 16-byte chunks, NaN codes patched (always:
+// a warp vote and a branch to skip the patch cost more than the patch).
 template <bool kScaled>
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 w, float sc, uint4& c0, uint4& c1) {
   e4m3x4_to_bf16<kScaled>(w.x, sc, c0.x, c0.y);
   e4m3x4_to_bf16<kScaled>(w.y, sc, c0.z, c0.w);
   e4m3x4_to_bf16<kScaled>(w.z, sc, c1.x, c1.y);
   e4m3x4_to_bf16<kScaled>(w.w, sc, c1.z, c1.w);
+  c0.x = nan_patch(c0.x, w.x, 0x1100u);
+  c0.y = nan_patch(c0.y, w.x, 0x3322u);
+  c0.z = nan_patch(c0.z, w.y, 0x1100u);
+  c0.w = nan_patch(c0.w, w.y, 0x3322u);
+  c1.x = nan_patch(c1.x, w.z, 0x1100u);
+  c1.y = nan_patch(c1.y, w.z, 0x3322u);
+  c1.z = nan_patch(c1.z, w.w, 0x1100u);
+  c1.w = nan_patch(c1.w, w.w, 0x3322u);
 }
 
 __device__ __forceinline__ int ntiles(const Seg& s) { return (s.k1 - s.k0 + kKeysT - 1) / kKeysT; }

@@ -227,3 +227,26 @@ def test_sparse_decode_single_slot_reads_every_code_exactly(mla):
     mla.mla_device_error()
     want = orc.ds_mla_values(entry[None, :])[0][0]
     assert np.array_equal(to_f64(o)[0], np.broadcast_to(want, (H, 512)))
+
+
+def test_fp8_decode_nan_code_poisons_only_its_sequence(mla):
+    # a NaN code in one sequence's cache makes that sequence's output NaN (the oracle's reading
+    # of a NaN code) and leaves the other sequences exact to the tolerance
+    import torch
+    H, L, R, page = 128, 512, 64, 64
+    E = L + R
+    lens = [200, 150]
+    codes, table = _fp8_batch(H, L, R, lens, page, 7601, 1.0)
+    blk = int(table[1, 1])
+    codes[blk, 7, 300] = 0x7F                                   # NaN, in sequence 1's rows
+    q_bits = mi.encode(mi.draw("normal", 7602, 2 * H * E, 0.3), "bf16").reshape(2, H, E)
+    o = poisoned((2, H, L), "bf16")
+    mla.mla_decode_fp8(o, to_dev(q_bits, "bf16"), _u8(codes), torch.from_numpy(table).cuda(),
+                       torch.from_numpy(np.array(lens, np.int32)).cuda(), L, R, 1.0 / math.sqrt(E))
+    mla.mla_device_error()
+    with np.errstate(invalid="ignore"):
+        want, _ = orc.decode_fp8(mi.decode_f64(q_bits, "bf16"), codes.reshape(-1), 0, page, (page * E, E, 1), L, R,
+                                 table, np.array(lens), 1.0 / math.sqrt(E), 1.0, 1.0)
+    got = to_f64(o)
+    assert np.all(np.isnan(want[1])) and np.all(np.isnan(got[1]))
+    check_close(got[0], want[0], "bf16", "fp8 decode next to a NaN sequence")
