@@ -711,6 +711,26 @@ def decode_figures(mla, mi, device, out, peaks, timed) -> None:
             del cache8, rows, slots
         del cache, q, o, ws
     del table, lens
+    # sparse top-2048 decode over an fp8 ds_mla cache: 64 queries of 128 heads, distinct slots
+    # scattered over 4096 blocks of 64 entries (172 MB), every slot list full
+    nrows = 4096 * 64
+    codes = torch.randint(0, 0x70, (nrows, 512), dtype=torch.uint8, device=device)
+    codes |= torch.randint(0, 2, (nrows, 512), dtype=torch.uint8, device=device) << 7
+    scales = (torch.rand((nrows, 4), device=device) * (1.0 / 32 - 1.0 / 128) + 1.0 / 128).view(torch.uint8)
+    rope = (torch.randn((nrows, 64), device=device) * 0.1).to(torch.bfloat16).view(torch.uint8)
+    view = torch.cat([codes, scales, rope], dim=1).view(4096, 64, 656)
+    del codes, scales, rope
+    idx = mi.permutation(8193, nrows)[: 64 * 2048].astype(np.int32).reshape(64, 2048)
+    qs = torch.randn((64, 128, 576), device=device).mul_(0.1).to(torch.bfloat16)
+    os_ = torch.empty((64, 128, 512), dtype=torch.bfloat16, device=device)
+    ind = torch.from_numpy(idx).to(device)
+    ms = timed(lambda: mla.mla_decode_sparse_fp8(os_, qs, view, ind, 576 ** -0.5), reps=10)
+    nbytes = 64 * 2048 * 656 + 64 * 128 * 576 * 2 + 64 * 128 * 512 * 2 + 64 * 2048 * 4
+    flops = 64 * 2048 * 128 * 2 * (576 + 512)
+    out["decode_sparse_fp8_b64_top2048"] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                                            "queries_per_s": 64 / (ms * 1e-3),
+                                            "roofline": roofline(nbytes, flops, ms, peaks)}
+    del view, qs, os_, ind
 
 
 def copy_figures(mla, mi, device, out, peaks, dev, device_timed, l2_bytes) -> None:
