@@ -129,3 +129,49 @@ def test_concat_in_place_without_rope_moves_nothing(mla):
     # the same with the q_cat_out of a rope-carrying layout still validates its widths first
     assert lib.mla_concat_q(1, _contig([T, H, L + 4]), _view([T, H, L], [H * (L + 4), L + 4, 1], 0x10000),
                             _contig([T, H, 3]), None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_fused_copy_fp8_sparse_and_vup_validation(mla):
+    # argument checks of the later entry points, all on the host before any launch
+    lib = mla.lib()
+    # concat + cache write in one call: each half is checked as its own call would be
+    cache = _contig([4, 16, 10])
+    assert lib.mla_concat_q_cache_write(1, _contig([4, 8, 10]), _contig([4, 8, 8]), _contig([4, 8, 3]), cache,
+                                        _contig([3, 8]), _contig([3, 2]), 0x1000, 3, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_concat_q_cache_write(1, _contig([4, 8, 10]), _contig([4, 8, 8]), _contig([4, 8, 2]), cache,
+                                        _contig([3, 8]), _contig([3, 3]), 0x1000, 3, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_concat_q_cache_write(1, _contig([0, 8, 10]), _contig([0, 8, 8]), _contig([0, 8, 2]), cache,
+                                        _contig([0, 8]), _contig([0, 2]), None, 0, None) == mla.MLA_OK
+    # e4m3 cache write: the scale is required
+    assert lib.mla_cache_write_fp8(1, _contig([4, 16, 10]), _contig([3, 8]), _contig([3, 2]), 0x1000, 3, None,
+                                   None) == mla.MLA_ERR_INVALID_ARG
+    # sparse ds_mla decode
+    B, H = 2, 16
+    q, o, c = _contig([B, H, 576]), _contig([B, H, 512]), _contig([8, 64, 656])
+
+    def sparse(o=o, q=q, c=c, idx=0x2000, ids=128, topk=128, ws=0x4000, wsb=1 << 30):
+        return lib.mla_decode_sparse_fp8(1, o, None, q, c, idx, ids, topk, 0.1, 0, ws, wsb, None)
+
+    assert sparse(q=_contig([B, H, 512])) == mla.MLA_ERR_INVALID_ARG          # not a 576-wide query
+    assert sparse(o=_contig([B, H, 256])) == mla.MLA_ERR_INVALID_ARG
+    assert sparse(c=_contig([8, 64, 576])) == mla.MLA_ERR_INVALID_ARG         # not a 656-byte entry
+    assert sparse(c=_view([8, 64, 656], [64 * 656, 656, 1], 0x10008)) == mla.MLA_ERR_INVALID_ARG   # unaligned
+    assert sparse(topk=-1) == mla.MLA_ERR_INVALID_ARG
+    assert sparse(idx=None) == mla.MLA_ERR_INVALID_ARG
+    assert sparse(ids=64) == mla.MLA_ERR_INVALID_ARG                           # row stride < top-k
+    assert sparse(wsb=16) == mla.MLA_ERR_INVALID_ARG
+    assert sparse(q=_contig([0, H, 576]), o=_contig([0, H, 512])) == mla.MLA_OK
+    assert lib.mla_decode_sparse_workspace_size(B, H, 128, 0) > lib.mla_decode_workspace_size(B, H, 512, 0)
+    # decode with the un-projection: out and w_uv must agree with the decode's shapes
+    L, R, V = 512, 64, 128
+    qv, cv = _contig([B, H, L + R]), _contig([8, 64, L + R])
+
+    def vup(out=_contig([B, H, V]), w=_contig([H, L, V]), ws=0x4000, wsb=1 << 30):
+        return lib.mla_decode_v_up(1, out, None, qv, cv, 0x2000, 4, 4, 0x3000, L, R, 0.1, w, 0, ws, wsb, None)
+
+    assert vup(out=_contig([B, H + 1, V])) == mla.MLA_ERR_INVALID_ARG
+    assert vup(w=_contig([H, L, V + 8])) == mla.MLA_ERR_INVALID_ARG
+    assert vup(w=_contig([H, L - 1, V])) == mla.MLA_ERR_INVALID_ARG
+    assert vup(wsb=1024) == mla.MLA_ERR_INVALID_ARG
+    assert b"workspace" in lib.mla_last_error()
+    assert lib.mla_decode_v_up_workspace_size(B, H, L, 0) >= lib.mla_decode_workspace_size(B, H, L, 0) + B * H * L * 2
