@@ -59,6 +59,7 @@
 // below 2^8.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
 
@@ -303,64 +304,30 @@ __device__ __forceinline__ float exp2_int(float d) {
   return d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
 }
 
-// e4m3 -> bf16 in shared memory. A code's exponent and mantissa bits placed in an fp32's
-// exponent and mantissa fields read as value * 2^-120 (an fp32 subnormal for exponent 0, which
-// the multiply honours), so one multiply by 2^120 gives every finite value exactly; the sign
-// bit goes to bit 31 first. Byte k of the word x is code k.
-__device__ __forceinline__ float e4m3_at(uint32_t x, int k, float mul) {
-  return __uint_as_float(((x << (24 - 8 * k)) & 0x80000000u) | (((x >> (8 * k)) << 20) & 0x07F00000u)) *
-         0x1p120f * mul;
-}
-
-// The two NaN codes (every exponent and mantissa bit set) would read as +-480: their bf16
-// halves are replaced by NaN. `sel` picks the two bytes of x that the packed word holds
-// (0x1100: bytes 0 and 1, 0x3322: bytes 2 and 3), each widened to its 16-bit half.
-__device__ __forceinline__ uint32_t nan_patch(uint32_t packed, uint32_t x, uint32_t sel) {
-  const uint32_t nan = ((x & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;   // bit 7: code is NaN
-  const uint32_t mask = __byte_perm((nan >> 7) * 0xFFu, 0u, sel);          // 0xFF per NaN byte
-  return (packed & ~mask) | (0x7FC07FC0u & mask);
-}
-
-// Two codes (bytes b0 and b1 of x, selected by `spread`) -> a bf16x2 word, exactly: the same
-// bit placement in bf16 lanes (value * 2^-120, a bf16 subnormal for exponent 0) times 2^120.
-__device__ __forceinline__ uint32_t e4m3x2_bf16(uint32_t x, uint32_t spread) {
-  const uint32_t t = __byte_perm(x, 0u, spread);   // code k in bits [16k, 16k + 8)
-  const uint32_t bits = ((t << 4) & 0x07F007F0u) | ((t << 8) & 0x80008000u);
-  const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&bits), __float2bfloat162_rn(0x1p120f));
+// e4m3 -> bf16 in shared memory. Two codes go to f16x2 in one hardware conversion (every e4m3
+// value, the NaN codes included, is exact in f16), each half widens to fp32 exactly, and one
+// pack rounds the pair to bf16x2: exact without a scale (e4m3 values are bf16 values), the
+// scaled product rounded once with one. Bits [16k, 16k + 16) of x hold codes 2k (low byte) and
+// 2k + 1.
+template <bool kScaled>
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float sc) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+  float lo = __half2float(__ushort_as_half(h.x)), hi = __half2float(__ushort_as_half(h.y));
+  if (kScaled) {
+    lo *= sc;
+    hi *= sc;
+  }
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Four codes -> two words of two bf16 each (low value first): exact, or with a scale each
-// product rounded to nearest.
-template <bool kScaled>
-__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t x, float sc, uint32_t& lo, uint32_t& hi) {
-  if (kScaled) {
-    const float f0 = e4m3_at(x, 0, sc), f1 = e4m3_at(x, 1, sc), f2 = e4m3_at(x, 2, sc), f3 = e4m3_at(x, 3, sc);
-    const __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
-    lo = *reinterpret_cast<const uint32_t*>(&a);
-    hi = *reinterpret_cast<const uint32_t*>(&b);
-  } else {
-    lo = e4m3x2_bf16(x, 0x4140u);   // bytes 0 and 1
-    hi = e4m3x2_bf16(x, 0x4342u);   // bytes 2 and 3
-  }
-}
-
-// 16 codes (one 16-byte granule) -> 16 bf16 as two 16-byte chunks, NaN codes patched (always:
-// a warp vote and a branch to skip the patch cost more than the patch).
+// 16 codes (one 16-byte granule) -> 16 bf16 as two 16-byte chunks, low code first.
 template <bool kScaled>
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 w, float sc, uint4& c0, uint4& c1) {
-  e4m3x4_to_bf16<kScaled>(w.x, sc, c0.x, c0.y);
-  e4m3x4_to_bf16<kScaled>(w.y, sc, c0.z, c0.w);
-  e4m3x4_to_bf16<kScaled>(w.z, sc, c1.x, c1.y);
-  e4m3x4_to_bf16<kScaled>(w.w, sc, c1.z, c1.w);
-  c0.x = nan_patch(c0.x, w.x, 0x1100u);
-  c0.y = nan_patch(c0.y, w.x, 0x3322u);
-  c0.z = nan_patch(c0.z, w.y, 0x1100u);
-  c0.w = nan_patch(c0.w, w.y, 0x3322u);
-  c1.x = nan_patch(c1.x, w.z, 0x1100u);
-  c1.y = nan_patch(c1.y, w.z, 0x3322u);
-  c1.z = nan_patch(c1.z, w.w, 0x1100u);
-  c1.w = nan_patch(c1.w, w.w, 0x3322u);
+  c0 = make_uint4(e4m3x2_to_bf16x2<kScaled>(w.x, sc), e4m3x2_to_bf16x2<kScaled>(w.x >> 16, sc),
+                  e4m3x2_to_bf16x2<kScaled>(w.y, sc), e4m3x2_to_bf16x2<kScaled>(w.y >> 16, sc));
+  c1 = make_uint4(e4m3x2_to_bf16x2<kScaled>(w.z, sc), e4m3x2_to_bf16x2<kScaled>(w.z >> 16, sc),
+                  e4m3x2_to_bf16x2<kScaled>(w.w, sc), e4m3x2_to_bf16x2<kScaled>(w.w >> 16, sc));
 }
 
 __device__ __forceinline__ int ntiles(const Seg& s) { return (s.k1 - s.k0 + kKeysT - 1) / kKeysT; }
