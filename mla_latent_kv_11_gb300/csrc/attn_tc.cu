@@ -50,7 +50,9 @@
 // warps 8..11 run the softmax, the O rescale and the epilogue, one thread per
 // query row (TMEM lane) in each group; warp 3 forwards the softmax group's
 // "incoming piece read" signals to the peer as relaxed remote arrives (the
-// reads they answer for were completed by a bar.sync). Every wait is bounded
+// reads they answer for were completed by a bar.sync). For e4m3 caches warps 0
+// and 2 convert staged tiles to bf16 instead, warp 3 issues the staging loads of
+// whole pages, and the softmax group sends its slot releases itself. Every wait is bounded
 // in time; a timeout winds the kernel down and reports MLA_ERR_TIMEOUT
 // instead of hanging.
 //
@@ -94,6 +96,9 @@ constexpr int kSoftmaxBar = 1;            // named barrier of the softmax warpgr
 constexpr int kXchgBar = 2;               // named barrier of the exchange warpgroup
 constexpr int kLoadBar = 3;               // named barrier of the loader warps (e4m3 caches)
 constexpr int kLoaders = 64;              // loader threads: warps 0 and 2
+// Dense e4m3 caches: warp 3 issues the staging TMA loads instead of forwarding the softmax
+// group's slot releases, which that group's first thread then sends to the peer itself.
+constexpr int kIssuerWarp = 3;
 constexpr float kLazyRescale = 8.0f;      // log2 units
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
@@ -163,10 +168,20 @@ __device__ long long g_trace_all[2][304][8][128];
     if (blockIdx.x < 304 && (g) < 128) g_trace_all[0][blockIdx.x][ev][(g)] = now_;    \
   } while (0)
 // loader events of work unit 0 (e4m3 caches)
-__device__ long long g_trace3[2][8][512];
+__device__ long long g_trace3[2][16][512];
 #define MLA_TRACE3_AT(ev, g)                                                   \
   do {                                                                          \
     if (unit == 0 && lt == 0 && (g) < 512) g_trace3[rank][ev][(g)] = clock64(); \
+  } while (0)
+// the same for the issuer warp's first thread
+#define MLA_TRACE3I_AT(ev, g)                                                     \
+  do {                                                                             \
+    if (unit == 0 && lane == 0 && (g) < 512) g_trace3[rank][ev][(g)] = clock64(); \
+  } while (0)
+// the same for the first thread of the second loader warp
+#define MLA_TRACE3B_AT(ev, g)                                                   \
+  do {                                                                           \
+    if (unit == 0 && lt == 32 && (g) < 512) g_trace3[rank][ev][(g)] = clock64(); \
   } while (0)
 #define MLA_TRACE2_AT(ev, g)                                                                  \
   do {                                                                                         \
@@ -183,6 +198,12 @@ __device__ long long g_trace3[2][8][512];
   } while (0)
 #define MLA_TRACE3_AT(ev, g) \
   do {                       \
+  } while (0)
+#define MLA_TRACE3B_AT(ev, g) \
+  do {                        \
+  } while (0)
+#define MLA_TRACE3I_AT(ev, g) \
+  do {                        \
   } while (0)
 #endif
 
@@ -514,9 +535,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int nt = 0, j = 0;           // tiles of the current segment, next tile in it
       bool have = false;           // a segment is open
       int gi = 0, gc = 0;          // tiles issued, tiles converted
-      int blk_pf = -1, blk_now = -1;   // block ids of the next 32 tiles (a lane each) and of this one
       bool ok = true, more = true;     // ok: the group's decision, the same in every loader thread
-      bool iss_ok = true;              // the issuing thread's own waits (TMA'd pages)
       while (ok) {
         // ---- issue: up to kStg tiles ahead of the conversion
         while (ok && more && gi < gc + C::kStg) {
@@ -533,55 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int u = gi % C::kStg;
           MLA_TRACE3_AT(0, gi);
           if (kSrc == 1 && p.fp8_tma) {
-            // whole pages of rows: one thread issues this CTA's latent box (and rope box) of every
-            // page the tile spans; rows past the segment and rows of a page that could not load
-            // are zeroed by the conversion (the slot's metadata says which). With pages of 64 rows
-            // or more, the lanes of warp 0 fetch the block ids of the next 32 tiles of the
-            // segment at once. The other loader threads do not wait here: a failed wait reaches
-            // them through the next group decision (the conversion's).
-            const int rows_box = min(p.page, kKeysT), subs = kKeysT / rows_box;
-            const int kt = sg.k0 + j * kKeysT;
-            if (subs == 1 && warp == 0) {
-              if ((j & 31) == 0) {
-                const int jj = j + lane;
-                blk_pf = jj < nt ? p.block_table[(int64_t)sg.b * p.bt_stride + (sg.k0 + jj * kKeysT) / p.page] : -1;
-              }
-              blk_now = __shfl_sync(0xffffffffu, blk_pf, j & 31);
-            }
-            if (lt == 0 && iss_ok) {
-              iss_ok = mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort);
-              if (iss_ok) {
-                int blks[8];
-                uint32_t bytes = 0;
-                int bad = 0;
-                for (int i = 0; i < subs; ++i) {
-                  const int key = kt + i * rows_box;
-                  blks[i] = -1;
-                  if (key >= sg.k1) continue;
-                  const int blk = subs == 1 ? blk_now : p.block_table[(int64_t)sg.b * p.bt_stride + key / p.page];
-                  if (blk < 0 || blk >= p.num_blocks) {
-                    atomicOr(&g_tc_err, kErrDeviceData);
-                    bad |= 1 << i;
-                    continue;
-                  }
-                  blks[i] = blk;
-                  bytes += (uint32_t)(rows_box * (256 + (kRope ? kRopeHalf : 0)));
-                }
-                int* meta = reinterpret_cast<int*>(smem + C::kOffRowBase);
-                meta[2 * u] = min(kKeysT, sg.k1 - kt);   // rows kept
-                meta[2 * u + 1] = bad;                   // bit i: page i of the tile did not load
-                mbar_arrive_expect_tx(&bars.stg_full[u], bytes);
-                unsigned char* dst = stg + u * C::kStgBytes;
-                const int row0 = subs == 1 ? kt % p.page : 0;
-                for (int i = 0; i < subs; ++i) {
-                  if (blks[i] < 0) continue;
-                  tma_load_3d(dst + i * rows_box * 256, &kvmap, &bars.stg_full[u], col0, row0, blks[i]);
-                  if (kRope)
-                    tma_load_3d(dst + kKeysT * 256 + i * rows_box * kRopeHalf, &ropemap, &bars.stg_full[u],
-                                512 + kRopeHalf * (int)rank, row0, blks[i]);
-                }
-              }
-            }
+            // whole pages: the issuer warp loads them; the loaders only count the tiles
           } else {
             ok = group_all(mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort));
             if (!ok) break;
@@ -634,10 +605,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- convert tile gc: staging slot u -> bf16 stage s
         const int u = gc % C::kStg, s = gc % C::kStages;
         MLA_TRACE3_AT(3, gc);
-        bool mine = iss_ok && mbar_wait(&bars.stg_full[u], (gc / C::kStg) & 1, abort);
+        bool mine = mbar_wait(&bars.stg_full[u], (gc / C::kStg) & 1, abort);
         MLA_TRACE3_AT(4, gc);
         ok = group_all(mine && mbar_wait(&bars.kv_empty[s], ((gc / C::kStages) & 1) ^ 1, abort));
         MLA_TRACE3_AT(5, gc);
+        MLA_TRACE3B_AT(10, gc);
         if (!ok) break;
         const unsigned char* src = stg + u * C::kStgBytes;
         unsigned char* dst = sKV + s * C::kStageBytes;
@@ -653,23 +625,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         auto dropped = [&](int r) { return r >= keep || ((bad >> (r >> box_shift)) & 1); };
         // latent: 16 codes per staged granule -> 16 bf16, two 16-byte chunks of box g / 4 (one
-        // loop per part, so the lanes of a warp never split between the two)
-#pragma unroll 2
-        for (int f = lt; f < kKeysT * 16; f += kLoaders) {
-          const int r = f >> 4, g = f & 15;
-          const unsigned char* row = src + r * G * 16;
-          uint4 w = *reinterpret_cast<const uint4*>(boxes ? src + r * 256 + g * 16 : row + g * 16);
-          if (boxes && dropped(r)) w = make_uint4(0u, 0u, 0u, 0u);
-          uint4 c0, c1;
-          if (kSrc == 1)
-            e4m3x16_to_bf16<false>(w, 1.f, c0, c1);
-          else
-            e4m3x16_to_bf16<true>(w, reinterpret_cast<const float*>(row + 16 * 16)[2 * (int)rank + g / 8], c0, c1);
-          unsigned char* bx = dst + (g >> 2) * kBoxBytesK + r * 128;
+        // loop per part, so the lanes of a warp never split between the two). A warp converts
+        // two rows at a time, each thread one fixed granule g of its row: lanes 4q..4q+3 take
+        // granules 4q..4q+3 of the even row, lanes 4q+4..4q+7 granules 4(q^1).. of the odd one,
+        // so every quarter-warp reads eight distinct 16-byte bank groups of a staged 256-byte
+        // row and writes eight distinct chunks of the swizzled stage (even ones for the even
+        // row, odd ones for the odd row)
+        {
+          const int l = lt & 31, half = (l >> 2) & 1;
+          const int g = 4 * ((l >> 3) ^ half) + (l & 3);
           const int j0 = (g & 3) * 2;
-          *reinterpret_cast<uint4*>(bx + ((j0 ^ (r & 7)) << 4)) = c0;
-          *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ (r & 7)) << 4)) = c1;
+          unsigned char* box = dst + (g >> 2) * kBoxBytesK;
+#pragma unroll 4
+          for (int r = 2 * (lt >> 5) + half; r < kKeysT; r += 4) {
+            const unsigned char* row = src + r * G * 16;
+            uint4 w = *reinterpret_cast<const uint4*>(boxes ? src + r * 256 + g * 16 : row + g * 16);
+            if (boxes && dropped(r)) w = make_uint4(0u, 0u, 0u, 0u);
+            uint4 c0, c1;
+            if (kSrc == 1)
+              e4m3x16_to_bf16<false>(w, 1.f, c0, c1);
+            else
+              e4m3x16_to_bf16<true>(w, reinterpret_cast<const float*>(row + 16 * 16)[2 * (int)rank + g / 8], c0, c1);
+            unsigned char* bx = box + r * 128;
+            *reinterpret_cast<uint4*>(bx + ((j0 ^ (r & 7)) << 4)) = c0;
+            *reinterpret_cast<uint4*>(bx + (((j0 + 1) ^ (r & 7)) << 4)) = c1;
+          }
         }
+        MLA_TRACE3_AT(7, gc);
+        MLA_TRACE3B_AT(8, gc);
         // rope: 64-byte rows of the rope box, 64-byte swizzle
         if (kRope) {
           constexpr int RG = kSrc == 1 ? 2 : 4;   // staged rope granules per row
@@ -693,14 +676,99 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
+        MLA_TRACE3_AT(9, gc);
         fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
         mbar_arrive(&bars.kv_full[s]);
         mbar_arrive(&bars.stg_empty[u]);
         MLA_TRACE3_AT(6, gc);
+        MLA_TRACE3B_AT(11, gc);
         ++gc;
       }
       cp_async_wait_all();   // never leave with copies in flight
       if (!ok) set_abort(bars, peer);
+    }
+  } else if (kSrc == 1 && warp == kIssuerWarp) {
+    if constexpr (kSrc == 1) {
+      // ------------------------------------------------------------ staging issuer (e4m3
+      // caches of whole pages): one thread loads this CTA's latent box (and rope box) of every
+      // page a tile spans into the tile's staging slot once the loaders have freed it, with
+      // the slot's metadata (rows kept, pages that did not load) for the conversion, which
+      // zeroes the rest. With pages of 64 rows or more the lanes fetch the block ids of the
+      // next 32 tiles of a segment at once. The same walk as the loaders': the same tiles in
+      // the same slots.
+      if (p.fp8_tma) {
+        unsigned char* stg = smem + C::kOffStg;
+        int* meta = reinterpret_cast<int*>(smem + C::kOffRowBase);
+        const int rows_box = min(p.page, kKeysT), subs = kKeysT / rows_box;
+        Walker wk;
+        wk.init(p, unit, nunits);
+        Seg sg;
+        int gi = 0;
+        bool ok = true;
+        while (ok && wk.next(p, sg)) {
+          const int nt = ntiles(sg);
+          int blk_pf = -1;
+          for (int j = 0; ok && j < nt; ++j, ++gi) {
+            const int u = gi % C::kStg;
+            const int kt = sg.k0 + j * kKeysT;
+            int blk_now = -1;
+            if (subs == 1) {
+              if ((j & 31) == 0) {
+                const int jj = j + lane;
+                blk_pf = jj < nt ? p.block_table[(int64_t)sg.b * p.bt_stride + (sg.k0 + jj * kKeysT) / p.page] : -1;
+              }
+              blk_now = __shfl_sync(0xffffffffu, blk_pf, j & 31);
+            }
+            if (lane == 0) {
+              MLA_TRACE3I_AT(13, gi);
+              ok = mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort);
+              MLA_TRACE3I_AT(14, gi);
+              if (ok) {
+                uint32_t bytes = 0;
+                int bad = 0, blk0 = -1;
+                for (int i = 0; i < subs; ++i) {   // pass 1: bytes and bad pages
+                  const int key = kt + i * rows_box;
+                  if (key >= sg.k1) continue;
+                  const int blk = subs == 1 ? blk_now : p.block_table[(int64_t)sg.b * p.bt_stride + key / p.page];
+                  if (blk < 0 || blk >= p.num_blocks) {
+                    atomicOr(&g_tc_err, kErrDeviceData);
+                    bad |= 1 << i;
+                    continue;
+                  }
+                  if (i == 0) blk0 = blk;
+                  bytes += (uint32_t)(rows_box * (256 + (kRope ? kRopeHalf : 0)));
+                }
+                meta[2 * u] = min(kKeysT, sg.k1 - kt);   // rows kept
+                meta[2 * u + 1] = bad;                   // bit i: page i of the tile did not load
+                mbar_arrive_expect_tx(&bars.stg_full[u], bytes);
+                unsigned char* dst = stg + u * C::kStgBytes;
+                const int row0 = subs == 1 ? kt % p.page : 0;
+                for (int i = 0; i < subs; ++i) {   // pass 2: the loads (block ids re-read: cached)
+                  const int key = kt + i * rows_box;
+                  if (key >= sg.k1 || ((bad >> i) & 1)) continue;
+                  const int blk = i == 0 ? blk0 : p.block_table[(int64_t)sg.b * p.bt_stride + key / p.page];
+                  tma_load_3d(dst + i * rows_box * 256, &kvmap, &bars.stg_full[u], col0, row0, blk);
+                  if (kRope)
+                    tma_load_3d(dst + kKeysT * 256 + i * rows_box * kRopeHalf, &ropemap, &bars.stg_full[u],
+                                512 + kRopeHalf * (int)rank, row0, blk);
+                }
+              }
+              MLA_TRACE3I_AT(15, gi);
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          }
+        }
+        if (!ok && lane == 0) set_abort(bars, peer);
+        // never leave with copies in flight: wait for the last phase issued to every slot
+        if (lane == 0) {
+          volatile int dummy = 0;
+          for (int u = 0; u < C::kStg; ++u) {
+            const int issued = gi / C::kStg + (u < gi % C::kStg ? 1 : 0);
+            if (issued > 0 && !mbar_wait(&bars.stg_full[u], (issued - 1) & 1, &dummy))
+              atomicOr(&g_tc_err, kErrTimeout);
+          }
+        }
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer. The whole
@@ -1083,7 +1151,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           named_bar(kSoftmaxBar, 128);
           if (row == 0) {
             mbar_arrive_expect_tx(&bars.x_full[rs], kXSlot);
-            mbar_arrive(&bars.xin_free[rs]);
+            if (kSrc == 1)   // no forwarder: release the slot to the peer directly (relaxed: the
+              mbar_arrive_remote_relaxed(&bars.x_empty[rs], peer);   // reads are behind the barrier)
+            else
+              mbar_arrive(&bars.xin_free[rs]);
             if (h == 0) mbar_arrive(&bars.xloc_free);
           }
           if (h == 0) {
