@@ -455,6 +455,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (ok && wk.next(p, sg)) {
       const int nt = ntiles(sg);
       const int32_t* bt = p.block_table + (int64_t)sg.b * p.bt_stride;
+      if (p.mode == 1) {
+        // prefill: the next row tile's queries (this CTA's 512 + 64 bytes of each of its rows)
+        // into L2 while this one runs, so the exchange group's Q load at its start finds them
+        // there; row tiles are short (about sixteen key tiles at 2048 tokens)
+        Walker wn = wk;
+        Seg sn;
+        if (wn.next(p, sn)) {
+          constexpr int kParts = kRope ? 5 : 4;   // 128-byte lines of a row's part
+          for (int i = lane; i < kRows * kParts; i += 32) {
+            const int r = i / kParts, part = i - r * kParts, t = r / p.H;
+            if (r < p.H * p.tpt && t < sn.ntok)
+              prefetch_l2(p.q + (int64_t)(sn.tok0 + t) * p.q_s0 + (int64_t)(r - t * p.H) * p.q_s1 +
+                          (part < 4 ? col0 + 64 * part : rope0));
+          }
+        }
+      }
       for (int j0 = 0; ok && j0 < nt; j0 += 32) {
         // lanes prefetch the block ids of the next 32 tiles (pages of >= 64 rows)
         int my_blk = 0;
@@ -954,6 +970,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t peer_xfull0 = map_to_rank(&bars.x_full[0], peer);
     // A named barrier has no timeout, so every decision is taken by all 128 threads.
     auto group_all = [](bool v) { return named_bar_and(kXchgBar, 128, v); };
+    auto prefetch_row = [&](const __nv_bfloat16* r) {   // this CTA's 512 + 64 bytes of a Q row
+#pragma unroll
+      for (int i = 0; i < 256; i += 64) prefetch_l2(r + col0 + i);
+      if (kRope) prefetch_l2(r + rope0);
+    };
     Walker wk;
     wk.init(p, unit, nunits);
     Seg sg;
@@ -970,36 +991,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (nt > 0) {
         const __nv_bfloat16* qrow = p.q + (int64_t)(sg.tok0 + t_in_tile) * p.q_s0 + (int64_t)head * p.q_s1;
-        for (int c = 0; c < 4; ++c) {
-          // latent chunk c: 64 values, 32 columns
-          const __nv_bfloat16* src = qrow + col0 + c * 64;
-          uint32_t v[32];
+        // The row's parts are read in five dependent rounds below; prefetched into L2 first,
+        // only the first round waits for DRAM
+        if (row_valid) prefetch_row(qrow);
+        // two rounds of loads: latent chunks 0 and 1, then chunks 2 and 3 with the rope part
+        // (a chunk: 64 values, 32 columns). This CTA's 32 rope values fill exactly 16 columns;
+        // the row-sum columns l follow them, and the softmax group may still be about to read
+        // the current segment's l, so nothing beyond the rope's 16 columns may be written here.
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_valid) w = *reinterpret_cast<const uint4*>(src + i * 8);
-            v[4 * i] = w.x;
-            v[4 * i + 1] = w.y;
-            v[4 * i + 2] = w.z;
-            v[4 * i + 3] = w.w;
-          }
-          tmem_st32u(tmem + lane_addr + kTmemQ + c * 32, v);
-        }
-        if (kRope) {
-          // this CTA's 32 rope values: exactly 16 columns. The row-sum columns l follow them, and
-          // the softmax group may still be about to read the current segment's l, so nothing
-          // beyond the rope's 16 columns may be written here.
-          uint32_t v[16];
+        for (int c2 = 0; c2 < 4; c2 += 2) {
+          uint32_t v[2][32];
+          uint32_t vr[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_valid) w = *reinterpret_cast<const uint4*>(qrow + rope0 + i * 8);
-            v[4 * i] = w.x;
-            v[4 * i + 1] = w.y;
-            v[4 * i + 2] = w.z;
-            v[4 * i + 3] = w.w;
+          for (int cc = 0; cc < 2; ++cc) {
+            const __nv_bfloat16* src = qrow + col0 + (c2 + cc) * 64;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint4 w = make_uint4(0, 0, 0, 0);
+              if (row_valid) w = *reinterpret_cast<const uint4*>(src + i * 8);
+              v[cc][4 * i] = w.x;
+              v[cc][4 * i + 1] = w.y;
+              v[cc][4 * i + 2] = w.z;
+              v[cc][4 * i + 3] = w.w;
+            }
           }
-          tmem_st16u(tmem + lane_addr + kTmemQ + 128, v);
+          if (kRope && c2 == 2) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w = make_uint4(0, 0, 0, 0);
+              if (row_valid) w = *reinterpret_cast<const uint4*>(qrow + rope0 + i * 8);
+              vr[4 * i] = w.x;
+              vr[4 * i + 1] = w.y;
+              vr[4 * i + 2] = w.z;
+              vr[4 * i + 3] = w.w;
+            }
+          }
+          tmem_st32u(tmem + lane_addr + kTmemQ + c2 * 32, v[0]);
+          tmem_st32u(tmem + lane_addr + kTmemQ + (c2 + 1) * 32, v[1]);
+          if (kRope && c2 == 2) tmem_st16u(tmem + lane_addr + kTmemQ + 128, vr);
         }
         tmem_st_wait();
         tc_fence_before();

@@ -161,6 +161,18 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// Bring `bytes` (a multiple of 16, from a 16-byte aligned address) of global memory into L2
+// without waiting: one operation of the tensor memory accelerator.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Bring the L2 line holding `src` into L2 without waiting (a load-store unit prefetch: it does
+// not queue behind the tensor memory accelerator's copies).
+__device__ __forceinline__ void prefetch_l2(const void* src) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+
 // ---------------------------------------------------------------- gathered copies
 // 16 bytes global -> shared through L2 (cp.async.cg); `src_bytes` < 16 fills the rest of the
 // 16 bytes with zeros (0: nothing is read, all zeros).

@@ -250,3 +250,47 @@ def test_fp8_decode_nan_code_poisons_only_its_sequence(mla):
     got = to_f64(o)
     assert np.all(np.isnan(want[1])) and np.all(np.isnan(got[1]))
     check_close(got[0], want[0], "bf16", "fp8 decode next to a NaN sequence")
+
+
+@pytest.mark.parametrize("H,R", [(128, 64), (64, 0)])
+@pytest.mark.parametrize("tiny", [False, True], ids=["huge_elements", "tiny_rows"])
+def test_fp8_decode_query_rows_of_any_magnitude(mla, H, R, tiny):
+    # The e4m3 path's queries must keep every row's scores as its bf16 values give them, whatever
+    # the row's magnitude. huge_elements: some rows hold one element of 2^18, 2^20 or -2^21 (beyond
+    # f16's range, so a conversion of the queries to f16 would fail them) in a column whose cache
+    # codes are all zero, so the scores stay ordinary; one row is zero. tiny_rows: every query
+    # times 2^-24 (below f16's smallest subnormal) with the softmax scale times 2^24, so the
+    # scores are the ordinary ones again.
+    import torch
+    L, page = 512, 64
+    E = L + R
+    lens = [300, 1000, 65]
+    B = len(lens)
+    codes, table = _fp8_batch(H, L, R, lens, page, 7701 + H, 1.0)
+    q = mi.draw("normal", 7702 + H, B * H * E, 0.3).reshape(B, H, E).astype(np.float64)
+    scale = 1.0 / math.sqrt(E)
+    if tiny:
+        q *= 2.0 ** -24
+        scale *= 2.0 ** 24
+    else:
+        cols = [100, 300] + ([520, 560] if R else [])        # both CTAs' halves, rope included
+        codes[:, :, cols] = 0
+        pick = mi.permutation(7703 + H, B * H).reshape(B, H)
+        for b in range(B):
+            for h in range(H):
+                k = pick[b, h] % 8
+                if k < 3:
+                    q[b, h, cols[pick[b, h] % len(cols)]] = (2.0 ** 18, 2.0 ** 20, -(2.0 ** 21))[k]
+        q[1, 5] = 0.0
+    q_bits = mi.to_bf16_bits(q.astype(np.float32))
+    want, want_lse = orc.decode_fp8(mi.decode_f64(q_bits, "bf16"), codes.reshape(-1), 0, page, (page * E, E, 1),
+                                    L, R, table, np.array(lens), scale, 1.0, 1.0)
+    o = poisoned((B, H, L), "bf16")
+    lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
+    mla.mla_decode_fp8(o, to_dev(q_bits, "bf16"), _u8(codes), torch.from_numpy(table).cuda(),
+                       torch.from_numpy(np.array(lens, np.int32)).cuda(), L, R, scale, lse_out=lse)
+    mla.mla_device_error()
+    check_close(to_f64(o), want, "bf16", f"fp8 decode, query magnitudes (tiny={tiny}), H={H} R={R}")
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got_lse))
+    assert np.max(np.abs(got_lse - want_lse)) < 1e-2
