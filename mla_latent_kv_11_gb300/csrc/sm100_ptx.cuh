@@ -161,6 +161,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// 32 bytes of global memory from a 32-byte aligned address, in one load.
+__device__ __forceinline__ void ld_global_32B(const void* src, uint32_t (&r)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(src)
+               : "memory");
+}
+
 // Bring `bytes` (a multiple of 16, from a 16-byte aligned address) of global memory into L2
 // without waiting: one operation of the tensor memory accelerator.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
