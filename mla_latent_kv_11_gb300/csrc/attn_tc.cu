@@ -400,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int u = 0; u < C::kStg; ++u) {
       // TMA boxes: one expect-tx arrival; gathers: one cp.async arrival per loader thread
-      mbar_init(&bars.stg_full[u], (kSrc == 1 && p.fp8_tma) ? 1 : kLoaders);
+      mbar_init(&bars.stg_full[u], (kSrc == 1 && p.fp8_tma) ? 1 : 32);
       mbar_init(&bars.stg_empty[u], kLoaders);
     }
     mbar_init(&bars.s_full, 1);
@@ -546,13 +546,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (kSrc != 0 && (warp == 0 || warp == 2)) {
     if constexpr (kSrc != 0) {
       // ------------------------------------------------------------ loader (e4m3 caches): 64
-      // threads gather this CTA's bytes of every key row with cp.async into a staging slot (rows
-      // past the segment are zero-filled), running up to kStg tiles ahead, and convert each landed
-      // tile to bf16 in the swizzled layout of a TMA box once its bf16 stage is free
+      // threads convert each tile that warp 3 has staged (up to kStg tiles ahead) to bf16 in the
+      // swizzled layout of a TMA box once its bf16 stage is free
       const int lt = (warp == 0 ? 0 : 32) + lane;
       constexpr int G = C::kGran;
       auto group_all = [](bool v) { return named_bar_and(kLoadBar, kLoaders, v); };
-      int64_t* rowbase = reinterpret_cast<int64_t*>(smem + C::kOffRowBase);
       unsigned char* stg = smem + C::kOffStg;
       Walker wk;
       wk.init(p, unit, nunits);
@@ -562,7 +560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int gi = 0, gc = 0;          // tiles issued, tiles converted
       bool ok = true, more = true;     // ok: the group's decision, the same in every loader thread
       while (ok) {
-        // ---- issue: up to kStg tiles ahead of the conversion
+        // ---- the tiles warp 3 issues, up to kStg ahead of the conversion
         while (ok && more && gi < gc + C::kStg) {
           while (!have || j >= nt) {
             if (!wk.next(p, sg)) {
@@ -574,56 +572,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             have = true;
           }
           if (!more) break;
-          const int u = gi % C::kStg;
-          MLA_TRACE3_AT(0, gi);
-          if (kSrc == 1 && p.fp8_tma) {
-            // whole pages: the issuer warp loads them; the loaders only count the tiles
-          } else {
-            ok = group_all(mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort));
-            if (!ok) break;
-            // byte offset of each row of the tile (-1: past the segment or a bad block id)
-            int64_t* rb = rowbase + (gi & 1) * kKeysT;
-            {
-              const int t = sg.k0 + j * kKeysT + lt;
-              int64_t off = -1;
-              if (t < sg.k1) {
-                if (kSrc == 1) {
-                  const int blk = p.block_table[(int64_t)sg.b * p.bt_stride + t / p.page];
-                  if (blk >= 0 && blk < p.num_blocks)
-                    off = (int64_t)blk * p.s_blk8 + (int64_t)(t % p.page) * p.s_row8;
-                  else
-                    atomicOr(&g_tc_err, kErrDeviceData);
-                } else {
-                  const int slot = p.slots[(int64_t)sg.b * p.slot_stride + t];   // compacted: in range
-                  off = (int64_t)(slot / p.page) * p.s_blk8 + (int64_t)(slot % p.page) * p.s_row8;
-                }
-              }
-              rb[lt] = off;
-            }
-            named_bar(kLoadBar, kLoaders);
-            MLA_TRACE3_AT(1, gi);
-            const uint32_t dst0 = smem_u32(stg + u * C::kStgBytes);
-            // the 16 latent granules of every row, then the tail granules (rope; and the scales
-            // of a ds_mla entry): one loop each, so no lane of a warp takes the other kind
-  #pragma unroll 4
-            for (int f = lt; f < kKeysT * 16; f += kLoaders) {
-              const int r = f >> 4, g = f & 15;
-              const int64_t off = rb[r];
-              cp_async16(dst0 + (r * G + g) * 16, p.cache8 + (off < 0 ? 0 : off + col0 + 16 * g), off < 0 ? 0u : 16u);
-            }
-            constexpr int TG = G > 16 ? G - 16 : 1;   // tail granules per row (none without rope)
-            for (int f = lt; f < kKeysT * (G - 16); f += kLoaders) {
-              const int r = f / TG, g = f - r * TG;
-              const int64_t off = rb[r];
-              const int byte = kSrc == 1 ? 512 + kRopeHalf * (int)rank + 16 * g
-                                         : (g == 0 ? kDsMlaLatent : kDsMlaRopeByte + 64 * (int)rank + 16 * (g - 1));
-              cp_async16(dst0 + (r * G + 16 + g) * 16, p.cache8 + (off < 0 ? 0 : off + byte), off < 0 ? 0u : 16u);
-            }
-            cp_async_commit();
-            cp_async_arrive_noinc(&bars.stg_full[u]);
-          }
-          MLA_TRACE3_AT(2, gi);
-          ++gi;
+          ++gi;   // warp 3 loads the tiles; the loaders only count them
           ++j;
         }
         if (!ok || gc == gi) break;
@@ -709,19 +658,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         MLA_TRACE3B_AT(11, gc);
         ++gc;
       }
-      cp_async_wait_all();   // never leave with copies in flight
       if (!ok) set_abort(bars, peer);
     }
-  } else if (kSrc == 1 && warp == kIssuerWarp) {
-    if constexpr (kSrc == 1) {
+  } else if (kSrc != 0 && warp == kIssuerWarp) {
+    if constexpr (kSrc != 0) {
       // ------------------------------------------------------------ staging issuer (e4m3
-      // caches of whole pages): one thread loads this CTA's latent box (and rope box) of every
+      // caches). Whole pages: one thread loads this CTA's latent box (and rope box) of every
       // page a tile spans into the tile's staging slot once the loaders have freed it, with
       // the slot's metadata (rows kept, pages that did not load) for the conversion, which
       // zeroes the rest. With pages of 64 rows or more the lanes fetch the block ids of the
       // next 32 tiles of a segment at once. The same walk as the loaders': the same tiles in
       // the same slots.
-      if (p.fp8_tma) {
+      if (kSrc == 1 && p.fp8_tma) {
         unsigned char* stg = smem + C::kOffStg;
         int* meta = reinterpret_cast<int*>(smem + C::kOffRowBase);
         const int rows_box = min(p.page, kKeysT), subs = kKeysT / rows_box;
@@ -793,6 +741,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               atomicOr(&g_tc_err, kErrTimeout);
           }
         }
+      } else {
+        // gathered rows (ds_mla slots; e4m3 pages a TMA box cannot take): the warp's 32 threads
+        // copy this CTA's granules of every row of a tile with 16-byte cp.async into its
+        // staging slot once the loaders have freed it (rows past the segment zero-filled by the
+        // copy's source size), each thread's copies then counted on the slot's barrier
+        constexpr int G = C::kGran;
+        int64_t* rowbase = reinterpret_cast<int64_t*>(smem + C::kOffRowBase);
+        unsigned char* stg = smem + C::kOffStg;
+        Walker wk;
+        wk.init(p, unit, nunits);
+        Seg sg;
+        int gi = 0;
+        bool ok = true;
+        while (ok && wk.next(p, sg)) {
+          const int nt = ntiles(sg);
+          for (int j = 0; ok && j < nt; ++j, ++gi) {
+            const int u = gi % C::kStg;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort));
+            if (!ok) break;
+            // byte offset of each row of the tile (-1: past the segment or a bad block id)
+            int64_t* rb = rowbase + (gi & 1) * kKeysT;
+            for (int r = lane; r < kKeysT; r += 32) {
+              const int t = sg.k0 + j * kKeysT + r;
+              int64_t off = -1;
+              if (t < sg.k1) {
+                if (kSrc == 1) {
+                  const int blk = p.block_table[(int64_t)sg.b * p.bt_stride + t / p.page];
+                  if (blk >= 0 && blk < p.num_blocks)
+                    off = (int64_t)blk * p.s_blk8 + (int64_t)(t % p.page) * p.s_row8;
+                  else
+                    atomicOr(&g_tc_err, kErrDeviceData);
+                } else {
+                  const int slot = p.slots[(int64_t)sg.b * p.slot_stride + t];   // compacted: in range
+                  off = (int64_t)(slot / p.page) * p.s_blk8 + (int64_t)(slot % p.page) * p.s_row8;
+                }
+              }
+              rb[r] = off;
+            }
+            __syncwarp();
+            const uint32_t dst0 = smem_u32(stg + u * C::kStgBytes);
+            // the 16 latent granules of every row, then the tail granules (rope; and the scales
+            // of a ds_mla entry): one loop each, so no lane of the warp takes the other kind
+#pragma unroll 4
+            for (int f = lane; f < kKeysT * 16; f += 32) {
+              const int r = f >> 4, g = f & 15;
+              const int64_t off = rb[r];
+              cp_async16(dst0 + (r * G + g) * 16, p.cache8 + (off < 0 ? 0 : off + col0 + 16 * g), off < 0 ? 0u : 16u);
+            }
+            constexpr int TG = G > 16 ? G - 16 : 1;   // tail granules per row (none without rope)
+            for (int f = lane; f < kKeysT * (G - 16); f += 32) {
+              const int r = f / TG, g = f - r * TG;
+              const int64_t off = rb[r];
+              const int byte = kSrc == 1 ? 512 + kRopeHalf * (int)rank + 16 * g
+                                         : (g == 0 ? kDsMlaLatent : kDsMlaRopeByte + 64 * (int)rank + 16 * (g - 1));
+              cp_async16(dst0 + (r * G + 16 + g) * 16, p.cache8 + (off < 0 ? 0 : off + byte), off < 0 ? 0u : 16u);
+            }
+            cp_async_commit();
+            cp_async_arrive_noinc(&bars.stg_full[u]);
+            __syncwarp();   // every lane has read this tile's offsets before the next tile's are written
+          }
+        }
+        if (!ok && lane == 0) set_abort(bars, peer);
+        cp_async_wait_all();   // never leave with copies in flight
       }
     }
   } else if (warp == 1) {
@@ -1222,7 +1233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           named_bar(kSoftmaxBar, 128);
           if (row == 0) {
             mbar_arrive_expect_tx(&bars.x_full[rs], kXSlot);
-            if (kSrc == 1)   // no forwarder: release the slot to the peer directly (relaxed: the
+            if (kSrc != 0)   // no forwarder: release the slot to the peer directly (relaxed: the
               mbar_arrive_remote_relaxed(&bars.x_empty[rs], peer);   // reads are behind the barrier)
             else
               mbar_arrive(&bars.xin_free[rs]);
