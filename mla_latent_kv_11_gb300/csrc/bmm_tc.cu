@@ -46,12 +46,6 @@ struct BmmCfg {
   static constexpr int kSmem = kBarOff + 256 + 1024;  // + barriers + alignment slack
 };
 
-__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int32_t c0, int32_t c1, int32_t c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 template <int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     bmm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,

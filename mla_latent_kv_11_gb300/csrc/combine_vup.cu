@@ -9,8 +9,8 @@
 // LSE weights (the combine kernel's arithmetic), an empty one is zero. One tcgen05 MMA chain
 // then computes out^T = W_UV[h]^T (M = 128 v, K = 512, an MN-major operand straight from the
 // TMA boxes) times o_lat^T (N = 64 sequences, K-major), fp32 in TMEM, and the epilogue
-// writes out[b, h, v-tile] in bf16. The o_lat rows are rounded to bf16 before the MMA, as
-// the separate combine and v_up do.
+// writes out[b, h, v-tile] in bf16 with one TMA store. The o_lat rows are rounded to bf16
+// before the MMA, as the separate combine and v_up do.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -39,8 +39,6 @@ constexpr int kSmemAlloc = kOffBar + 64 + 2 * kSeqs * 4 + 1024;   // + barriers,
 constexpr uint32_t kTmemCols = 64;
 
 struct CvuParams {
-  __nv_bfloat16* out;            // [B, H, V], v contiguous
-  int64_t out_s0, out_s1;
   const __nv_bfloat16* o_lat;    // [B, H, L] rows of sequences held whole by one unit
   int64_t o_s0, o_s1;
   float* lse;                    // [B, H] or null
@@ -49,7 +47,8 @@ struct CvuParams {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    combine_vup_kernel(const __grid_constant__ CUtensorMap wmap, const CvuParams p) {
+    combine_vup_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap omap,
+                       const CvuParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
@@ -221,24 +220,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) atomicOr(&g_cvu_err, kErrTimeout);
   }
   if (warp < 4) {
-    // ---- epilogue: TMEM lane = v row of the tile, column = sequence of the chunk
+    // ---- epilogue: TMEM lane = v row of the tile, column = sequence of the chunk. The tile is
+    // staged as [64 sequences x 128 v] bf16 in the o_lat buffer (the MMA has read it) and goes
+    // out in one TMA store, which drops sequences past B
     const bool ok = mbar_wait(mma_done, 0, abort) && *abort == 0;   // no MMA ran if the weight never landed
     tc_fence_after();
     if (ok) {
       const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-      const int v = vt * kVT + warp * 32 + lane;
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sO);
+      const int vl = warp * 32 + lane;
       for (int c = 0; c < kSeqs; c += 32) {
         float d[32];
         tmem_ld32(tmem + lane_addr + c, d);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int b = b0 + c + i;
-          if (b < p.B) p.out[(int64_t)b * p.out_s0 + (int64_t)h * p.out_s1 + v] = __float2bfloat16_rn(d[i]);
-        }
+        for (int i = 0; i < 32; ++i) stage[(c + i) * kVT + vl] = __float2bfloat16_rn(d[i]);
       }
-    } else if (lane == 0) {
-      atomicOr(&g_cvu_err, kErrTimeout);
+      fence_proxy_async_smem();   // the TMA store reads the stage through the async proxy
+    }
+    const bool all_ok = named_bar_and(1, 128, ok);
+    if (tid == 0) {
+      if (all_ok) {
+        tma_store_3d(&omap, sO, vt * kVT, h, b0);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      } else {
+        atomicOr(&g_cvu_err, kErrTimeout);
+      }
     }
   }
   if (tid == 0 && *abort) {
@@ -260,7 +268,9 @@ bool combine_vup_supported(mla_dtype dt, int L, int V, const View3& out, const V
   if (dt != MLA_BF16 || L != kL || V % kVT != 0 || !tensor_maps_available()) return false;
   if (out.s2 != 1 || w_uv.s2 != 1) return false;
   auto al16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
-  return al16(w_uv.data) && w_uv.s0 % 8 == 0 && w_uv.s1 % 8 == 0;
+  // both go through tensor maps: 16-byte aligned bases and strides
+  return al16(w_uv.data) && w_uv.s0 % 8 == 0 && w_uv.s1 % 8 == 0 && al16(out.data) && out.s0 % 8 == 0 &&
+         out.s1 % 8 == 0;
 }
 
 cudaError_t launch_combine_vup(const View3& out, const View3& o_lat, float* lse, const View3& w_uv, int32_t B,
@@ -270,10 +280,12 @@ cudaError_t launch_combine_vup(const View3& out, const View3& o_lat, float* lse,
   if (!make_map3d(&wmap, w_uv.data, (uint64_t)V, kL, (uint64_t)H, (uint64_t)w_uv.s1 * 2, (uint64_t)w_uv.s0 * 2, 64,
                   64, 1, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  CUtensorMap omap;
+  // out as [B, H, V]: dims (V, H, B), box 128 v x 1 head x 64 sequences, no swizzle
+  if (!make_map3d(&omap, out.data, (uint64_t)V, (uint64_t)H, (uint64_t)B, (uint64_t)out.s1 * 2, (uint64_t)out.s0 * 2,
+                  kVT, 1, kSeqs, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   CvuParams p;
-  p.out = static_cast<__nv_bfloat16*>(out.data);
-  p.out_s0 = out.s0;
-  p.out_s1 = out.s1;
   p.o_lat = static_cast<const __nv_bfloat16*>(o_lat.data);
   p.o_s0 = o_lat.s0;
   p.o_s1 = o_lat.s1;
@@ -285,7 +297,7 @@ cudaError_t launch_combine_vup(const View3& out, const View3& o_lat, float* lse,
   cudaError_t e = cudaFuncSetAttribute(combine_vup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)H, (unsigned)(V / kVT), (unsigned)((B + kSeqs - 1) / kSeqs));
-  return launch_k(combine_vup_kernel, grid, dim3(kThreads), kSmemAlloc, st, wmap, p);
+  return launch_k(combine_vup_kernel, grid, dim3(kThreads), kSmemAlloc, st, wmap, omap, p);
 }
 
 unsigned combine_vup_errors_read_clear() {

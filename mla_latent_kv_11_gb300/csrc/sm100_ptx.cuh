@@ -203,6 +203,14 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src,
                ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
                : "memory");
 }
+// TMA store of a shared-memory box to the tile of a 3-D tensor map at (c0, c1, c2); elements
+// outside the tensor are not written. Completion: bulk_commit_group / bulk_wait_read_all.
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
