@@ -84,11 +84,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int vg = 0; vg < 2; ++vg)
         tma_load_3d(sW + (kc * 2 + vg) * kWBox, &wmap, w_full, vt * kVT + 64 * vg, 64 * kc, h);
   }
-  pdl_enter();   // o_lat rows, partials and the schedule come from the kernels before
-
-  // ---- o_lat rows of the chunk for head h, bf16, as K-major [64 seq x 64 l] boxes with
-  // 128-byte swizzle; lane owns columns lane*4 + 128k (k = 0..3). The loads are batched so a
-  // warp waits about one memory latency per phase, not one per sequence.
+  // Each sequence's piece count and first partial slot come from the schedule kernel two
+  // launches back, which had completed before this kernel could launch: the split kernel in
+  // between waits for it (griddepcontrol.wait) before it lets this kernel launch. They are
+  // read before this kernel's own wait; the o_lat rows and partials, the split kernel's
+  // output, only after it.
   int* s_np = reinterpret_cast<int*>(abort_flag + 1);   // [kSeqs] pieces of each sequence
   int* s_base = s_np + kSeqs;                              // [kSeqs] its first partial slot
   if (tid < kSeqs) {
@@ -96,7 +96,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_np[tid] = b < p.B ? p.s.npieces[b] : 0;
     s_base[tid] = b < p.B ? p.s.piece_base[b] : 0;
   }
+  pdl_enter();   // o_lat rows and partials come from the split kernel before
   __syncthreads();
+
+  // ---- o_lat rows of the chunk for head h, bf16, as K-major [64 seq x 64 l] boxes with
+  // 128-byte swizzle; lane owns columns lane*4 + 128k (k = 0..3). The loads are batched so a
+  // warp waits about one memory latency per phase, not one per sequence.
   auto store_row = [&](int n, const uint32_t (&w2)[4][2]) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
