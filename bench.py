@@ -224,14 +224,13 @@ class DecodeStep:
         m = self.mla
         out = self.out if out is None else out
         q_nope = self.q_nope if q_nope is None else q_nope
-        # the absorb writes q_lat straight into q_cat's first L columns (a [H,B,L] view of it),
-        # so the concat finds its nope operand in place and moves only the rope columns, in the
-        # same launch as the cache write of the new rows
-        lat = self.q_cat[:, :, :self.L]
-        m.mla_absorb_q(lat.transpose(0, 1), q_nope.transpose(0, 1), self.w_uk)
-        m.mla_concat_q_cache_write(self.q_cat, lat, self.q_pe if q_pe is None else q_pe, self.cache,
-                                   self.new_kv_c if kv_c is None else kv_c,
-                                   self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
+        # one call for steps 1 to 3: the absorb writes q_lat straight into q_cat's first L
+        # columns, and the rope columns of q_cat and the cache write of the new rows run in one
+        # launch alongside it
+        m.mla_absorb_concat_cache_write(self.q_cat, q_nope.transpose(0, 1), self.w_uk,
+                                        self.q_pe if q_pe is None else q_pe, self.cache,
+                                        self.new_kv_c if kv_c is None else kv_c,
+                                        self.new_k_pe if k_pe is None else k_pe, self.slots if slots is None else slots)
         if ev_decode is not None:
             ev_decode[0].record()
         m.mla_decode_v_up(out, self.q_cat, self.cache, self.table if table is None else table,

@@ -10,7 +10,10 @@
  *   mla_decode      o_lat = softmax(scale * q_cat . cache) c_kv    (step 4)
  *   mla_v_up        out[h,b,:]   = o_lat[h,b,:] @ W_UV[h]          (step 5)
  *
- * and mla_prefill is step 4 for many causal queries per sequence.
+ * and mla_prefill is step 4 for many causal queries per sequence. Fused forms:
+ * mla_concat_q_cache_write (steps 2 and 3 in one launch), mla_absorb_concat_cache_write
+ * (steps 1 to 3 in one call, the copies alongside the absorb) and mla_decode_v_up (step 4
+ * with step 5 in its combine).
  *
  * Sources of the operations (web pages):
  *   [vt]    vllm.cpp, tests/vt/test_ops_mla_absorb.cpp (BatchedMatmul and
@@ -170,6 +173,26 @@ mla_status mla_concat_q_cache_write(mla_dtype dtype, mla_tensor q_cat_out, mla_t
                                     mla_tensor rope, mla_tensor cache, mla_tensor kv_c,
                                     mla_tensor k_pe, const int64_t* slot_mapping,
                                     int64_t num_tokens, void* stream);
+
+/* Steps 1, 2 and 3 of a decode step in one call - the absorb straight into q_cat, the
+ * rope columns of q_cat and the cache write of the new rows (the fused pre-attention of the
+ * vllm.cpp and memra pages' step order, absorb -> q_cat included).
+ *   q_cat [T,H,L+R] (written), q_nope [H,T,P] (any strides with innermost 1: usually the
+ *   transpose of a [T,H,P] buffer), w_uk [H,P,L], q_pe [T,H,R] or [T,1,R]; cache, kv_c,
+ *   k_pe, slot_mapping and num_tokens as for mla_cache_write. One dtype for all tensors.
+ *   Results are exactly those of mla_absorb_q(q_cat's first L columns seen as [H,T,L],
+ *   q_nope, w_uk) followed by mla_concat_q_cache_write(q_cat, q_cat's own first L columns,
+ *   q_pe, cache, kv_c, k_pe, slot_mapping, num_tokens), and so are the errors (a w_uk wider
+ *   than q_cat, or shapes that do not match, return MLA_ERR_INVALID_ARG). The copies touch
+ *   only q_cat's rope columns and the cache, none of the absorb's operands or output, so on
+ *   the GPU they run alongside the absorb instead of after it; the call's work is complete,
+ *   as a whole, before anything queued after it on the stream starts reading it. q_cat,
+ *   q_nope, w_uk, q_pe, the cache, kv_c and k_pe must not overlap one another. */
+mla_status mla_absorb_concat_cache_write(mla_dtype dtype, mla_tensor q_cat, mla_tensor q_nope,
+                                         mla_tensor w_uk, mla_tensor q_pe, mla_tensor cache,
+                                         mla_tensor kv_c, mla_tensor k_pe,
+                                         const int64_t* slot_mapping, int64_t num_tokens,
+                                         void* stream);
 
 /* Step 3, fp8 cache - the cache write into an e4m3 cache ([vllm] concat_and_cache_mla
  * with a quantized cache dtype and its scale).

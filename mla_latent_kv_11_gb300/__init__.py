@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
                                    ctypes.c_int),
             "mla_cache_write_fp8": ([ctypes.c_int, T, T, T, P, I64, P, P], ctypes.c_int),
             "mla_concat_q_cache_write": ([ctypes.c_int, T, T, T, T, T, T, P, I64, P], ctypes.c_int),
+            "mla_absorb_concat_cache_write": ([ctypes.c_int, T, T, T, T, T, T, T, P, I64, P], ctypes.c_int),
             "mla_decode_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, P, I32, I32, F32, P, P, I32, P, SZ, P],
                                ctypes.c_int),
             "mla_decode_sparse_fp8": ([ctypes.c_int, T, P, T, T, P, I64, I32, F32, I32, P, SZ, P], ctypes.c_int),
@@ -203,6 +204,22 @@ def mla_concat_q_cache_write(q_cat_out, nope, rope, cache, kv_c, k_pe, slot_mapp
                                           as_mla_tensor(q_cat_out), as_mla_tensor(nope), as_mla_tensor(rope),
                                           as_mla_tensor(cache), as_mla_tensor(kv_c), as_mla_tensor(k_pe),
                                           _ptr(slot_mapping), slot_mapping.numel(), _stream(stream)))
+
+
+def mla_absorb_concat_cache_write(q_cat, q_nope, w_uk, q_pe, cache, kv_c, k_pe, slot_mapping, stream=None) -> None:
+    """Steps 1 to 3 in one call: mla_absorb_q into q_cat's first L columns (q_nope [H,T,P],
+    w_uk [H,P,L]), then the rope columns of q_cat and the cache write of the new rows, the
+    copies running alongside the absorb."""
+    import torch
+    if slot_mapping.dtype != torch.int64:
+        raise MlaError(MLA_ERR_INVALID_ARG, "slot_mapping must be int64")
+    if slot_mapping.numel() and not slot_mapping.is_contiguous():
+        raise MlaError(MLA_ERR_INVALID_ARG, "slot_mapping must be contiguous")
+    _check(lib().mla_absorb_concat_cache_write(_dtype_code(q_cat, q_nope, w_uk, q_pe, cache, kv_c, k_pe),
+                                               as_mla_tensor(q_cat), as_mla_tensor(q_nope), as_mla_tensor(w_uk),
+                                               as_mla_tensor(q_pe), as_mla_tensor(cache), as_mla_tensor(kv_c),
+                                               as_mla_tensor(k_pe), _ptr(slot_mapping), slot_mapping.numel(),
+                                               _stream(stream)))
 
 
 def mla_decode_workspace_size(batch: int, num_heads: int, kv_lora_rank: int, num_splits: int = 0) -> int:

@@ -220,8 +220,12 @@ struct CacheArgs {
   RowSplit rs;
 };
 
+template <bool kAlongside>
 __global__ void __launch_bounds__(256) concat_cache_kernel(ConcatArgs a, CacheArgs c, int q_blocks) {
-  pdl_enter();
+  if (kAlongside)
+    pdl_allow_dependents();   // the kernel before writes nothing this one touches (see the launcher)
+  else
+    pdl_enter();
   const bool q_part = (int)blockIdx.x < q_blocks;
   const int part_block = q_part ? blockIdx.x : blockIdx.x - q_blocks;
   const int part_blocks = q_part ? q_blocks : gridDim.x - q_blocks;
@@ -258,6 +262,8 @@ __global__ void __launch_bounds__(256) concat_cache_kernel(ConcatArgs a, CacheAr
       copy_row(o, kr, pr, c.Lw, Ew, c0, rs.G);
     }
   }
+  // alongside: complete only once the kernel before is, so the next kernel's wait covers both
+  if (kAlongside) pdl_wait();
 }
 
 
@@ -354,7 +360,7 @@ cudaError_t launch_cache_write_fp8(mla_dtype src_dt, const View3& cache, const V
 
 cudaError_t launch_concat_cache(mla_dtype dt, const View3& out, const View3& nope, const View3& rope,
                                 const View3& cache, const View3& kv_c, const View3& k_pe, int64_t L, int64_t R,
-                                const int64_t* slots, int64_t T, cudaStream_t st) {
+                                const int64_t* slots, int64_t T, cudaStream_t st, bool alongside) {
   const int64_t es = dt == MLA_F32 ? 4 : 2;
   const int64_t per = 16 / es;
   const int64_t Tq = out.n0, H = out.n1, Lq = nope.n2, Rq = rope.n2;
@@ -403,7 +409,7 @@ cudaError_t launch_concat_cache(mla_dtype dt, const View3& out, const View3& nop
   c.T = T;
   c.rs = row_split((L + R) / per);
   const int qb = grid_for(qrows, a.rs), cb = grid_for(T, c.rs);
-  return launch_k(concat_cache_kernel, qb + cb, 256, 0, st, a, c, qb);
+  return launch_k(alongside ? concat_cache_kernel<true> : concat_cache_kernel<false>, qb + cb, 256, 0, st, a, c, qb);
 }
 
 unsigned copy_errors_read_clear() {

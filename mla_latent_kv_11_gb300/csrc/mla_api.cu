@@ -379,6 +379,50 @@ mla_status mla_concat_q_cache_write(mla_dtype dtype, mla_tensor q_cat_out, mla_t
                      "mla_concat_q_cache_write");
 }
 
+mla_status mla_absorb_concat_cache_write(mla_dtype dtype, mla_tensor q_cat, mla_tensor q_nope, mla_tensor w_uk,
+                                         mla_tensor q_pe, mla_tensor cache, mla_tensor kv_c, mla_tensor k_pe,
+                                         const int64_t* slot_mapping, int64_t num_tokens, void* stream) {
+  g_msg[0] = 0;
+  MLA_TRY(check_dtype(dtype));
+  MLA_TRY(check_view(q_cat, 3, "q_cat"));
+  MLA_TRY(check_view(w_uk, 3, "w_uk"));
+  const int64_t L = w_uk.shape[2];
+  if (L > q_cat.shape[2])
+    return fail(MLA_ERR_INVALID_ARG, "w_uk's latent width %lld exceeds q_cat's width %lld", (long long)L,
+                (long long)q_cat.shape[2]);
+  // the absorb writes q_cat's first L columns, seen as [H, T, L]
+  mla_tensor lat = q_cat;
+  lat.shape[0] = q_cat.shape[1];
+  lat.shape[1] = q_cat.shape[0];
+  lat.shape[2] = L;
+  lat.stride[0] = q_cat.stride[1];
+  lat.stride[1] = q_cat.stride[0];
+  MLA_TRY(check_bmm(lat, q_nope, w_uk, "q_cat", "q_nope", "w_uk"));
+  // the concat with q_cat's own first L columns as its nope operand: only the rope moves
+  mla_tensor nope = q_cat;
+  nope.shape[2] = L;
+  ConcatPlan cp;
+  MLA_TRY(plan_concat(dtype, q_cat, nope, q_pe, &cp));
+  WritePlan wp;
+  MLA_TRY(plan_cache_write(dtype, cache, kv_c, k_pe, slot_mapping, num_tokens, &wp));
+  const cudaStream_t st = (cudaStream_t)stream;
+  const bool absorb = numel(lat) > 0;
+  if (absorb) MLA_TRY(cuda_status(launch_bmm(dtype, view3(lat), view3(q_nope), view3(w_uk), st),
+                                  "mla_absorb_concat_cache_write absorb"));
+  if (cp.empty && wp.empty) return MLA_OK;
+  View3 out = cp.out, nv = cp.nope, rv = cp.rope;
+  if (cp.empty) {   // nothing to concatenate: an empty q part
+    out.n0 = 0;
+    nv.n2 = 0;
+    rv.n2 = 0;
+  }
+  // the copies touch q_cat's rope columns and the cache, none of the absorb's operands or its
+  // output: they run alongside it
+  return cuda_status(launch_concat_cache(dtype, out, nv, rv, wp.cache, wp.kv_c, wp.k_pe, wp.L, wp.R, slot_mapping,
+                                         wp.empty ? 0 : num_tokens, st, absorb),
+                     "mla_absorb_concat_cache_write copies");
+}
+
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t kv_lora_rank,
                                  int32_t num_splits) {
   if (batch < 0 || num_heads < 0 || kv_lora_rank < 0 || num_splits < 0) return 0;

@@ -49,9 +49,13 @@ struct View3 {
 // visible (at once if the preceding stream work was not a programmatic launch), and
 // launch_dependents then lets the next kernel start launching.
 #ifdef __CUDACC__
-__device__ __forceinline__ void pdl_enter() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_allow_dependents();
 }
 #endif
 
@@ -211,9 +215,14 @@ mla_status plan_cache_write(mla_dtype dtype, const mla_tensor& cache, const mla_
                             const mla_tensor& k_pe, const int64_t* slot_mapping, int64_t num_tokens,
                             WritePlan* out);
 // The q concat and the cache write in one launch when both take 16-byte words, else two.
+// `alongside`: the launch directly follows a kernel of the same call that writes none of this
+// one's inputs or outputs and waits for its own predecessors before it lets dependents launch
+// (the absorb into q_cat's latent columns); the copies then run alongside it and wait for it
+// only before this kernel ends, so whatever follows still sees both complete.
 cudaError_t launch_concat_cache(mla_dtype dt, const View3& out, const View3& nope, const View3& rope,
                                 const View3& cache, const View3& kv_c, const View3& k_pe, int64_t L, int64_t R,
-                                const int64_t* slots, int64_t T, cudaStream_t st);
+                                const int64_t* slots, int64_t T, cudaStream_t st,
+                                bool alongside = false);
 
 // Work units of the general (CUDA-core) split-KV decode: num_splits, or two per SM.
 int32_t decode_units(int32_t num_splits);

@@ -175,3 +175,32 @@ def test_fused_copy_fp8_sparse_and_vup_validation(mla):
     assert vup(wsb=1024) == mla.MLA_ERR_INVALID_ARG
     assert b"workspace" in lib.mla_last_error()
     assert lib.mla_decode_v_up_workspace_size(B, H, L, 0) >= lib.mla_decode_workspace_size(B, H, L, 0) + B * H * L * 2
+
+
+def test_absorb_concat_cache_write_validation(mla):
+    # steps 1 to 3 in one call: every part is checked as its own call would be, on the host,
+    # before anything is launched (all of these fail or return before touching the device)
+    lib = mla.lib()
+    T, H, P, L, R = 4, 8, 16, 32, 8
+    q_cat = _contig([T, H, L + R])
+    q_nope = _view([H, T, P], [P, H * P, 1], 0x20000)     # the transpose of a [T,H,P] buffer
+    cache = _contig([4, 16, L + R])
+
+    def call(q_cat=q_cat, q_nope=q_nope, w_uk=_contig([H, P, L]), q_pe=_contig([T, H, R]), cache=cache,
+             kv_c=_contig([3, L]), k_pe=_contig([3, R]), slots=0x1000, n=3):
+        return lib.mla_absorb_concat_cache_write(1, q_cat, q_nope, w_uk, q_pe, cache, kv_c, k_pe, slots, n, None)
+
+    assert call(w_uk=_contig([H, P, L + R + 1])) == mla.MLA_ERR_INVALID_ARG   # wider than q_cat
+    assert call(w_uk=_contig([H, P + 1, L])) == mla.MLA_ERR_INVALID_ARG       # inner dimension
+    assert call(w_uk=_contig([H - 1, P, L])) == mla.MLA_ERR_INVALID_ARG       # heads
+    assert call(q_nope=_view([H, T + 1, P], [P, H * P, 1], 0x20000)) == mla.MLA_ERR_INVALID_ARG
+    assert call(q_pe=_contig([T, H, R + 1])) == mla.MLA_ERR_INVALID_ARG      # L + R != q_cat width
+    assert call(k_pe=_contig([3, R + 1])) == mla.MLA_ERR_INVALID_ARG         # cache entry width
+    assert call(slots=None) == mla.MLA_ERR_INVALID_ARG
+    assert call(n=-1) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_absorb_concat_cache_write(3, q_cat, q_nope, _contig([H, P, L]), _contig([T, H, R]), cache,
+                                             _contig([3, L]), _contig([3, R]), 0x1000, 3, None) == \
+        mla.MLA_ERR_INVALID_ARG                                                 # no such dtype
+    # nothing to do: no tokens, no rows to write
+    assert call(q_cat=_contig([0, H, L + R]), q_nope=_view([H, 0, P], [P, H * P, 1], 0x20000),
+                q_pe=_contig([0, H, R]), kv_c=_contig([0, L]), k_pe=_contig([0, R]), slots=None, n=0) == mla.MLA_OK

@@ -219,3 +219,55 @@ def test_concat_and_cache_write_in_one_launch_edges(mla, dtype, case):
     assert np.array_equal(to_host_bits(out).view(u), orc.concat_q(nope, rope).view(u))
     want = orc.cache_write(fill, 0, nb, page, (page * E, E, 1), kv, kp, slots)
     assert np.array_equal(to_host_bits(cache).reshape(-1).view(u), want.view(u))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", FUSED_CASES, ids=["v3_b64", "v2lite_bcast", "odd"])
+@pytest.mark.parametrize("bad_slot", [False, True], ids=["slots_ok", "slot_past_cache"])
+def test_absorb_concat_cache_write_in_one_call(mla, dtype, case, bad_slot):
+    # Steps 1 to 3 in one call (the copies alongside the absorb): the latent columns of q_cat
+    # are the oracle's product and bit-identical to mla_absorb_q into a buffer of its own, the
+    # rope columns and the whole unified cache buffer (its other layers' sentinels included)
+    # are the oracle's, bit for bit; a slot past the cache is reported and skipped.
+    import math
+    import torch
+    from helpers import check_close, to_f64
+    H, B, K, L, R, Hr = case
+    qn = mi.encode(mi.draw("uniform", 91, B * H * K), dtype).reshape(B, H, K)
+    w = mi.encode(mi.draw("uniform", 92, H * K * L, 1.0 / math.sqrt(K)), dtype).reshape(H, K, L)
+    rope = _bits(mi.normal(93, B * Hr * R), dtype).reshape(B, Hr, R)
+    nb, page, n_layers, layer = 6, 16, 3, 1
+    E = L + R
+    ntok = 21
+    kv = _bits(mi.normal(94, ntok * L), dtype).reshape(ntok, L)
+    kp = _bits(mi.normal(95, ntok * R), dtype).reshape(ntok, R)
+    slots = mi.permutation(96, nb * page)[:ntok].copy()
+    slots[3] = -1                                              # padding: writes nothing
+    if bad_slot:
+        slots[7] = nb * page + 2
+    fill = _bits(mi.normal(97, nb * n_layers * page * E), dtype)
+    big = to_dev(fill, dtype)
+    view = big.as_strided((nb, page, E), (n_layers * page * E, E, 1), layer * page * E)
+    q_cat = poisoned((B, H, E), dtype)
+    mla.mla_absorb_concat_cache_write(q_cat, to_dev(qn, dtype).transpose(0, 1), to_dev(w, dtype), to_dev(rope, dtype),
+                                      view, to_dev(kv, dtype), to_dev(kp, dtype), torch.from_numpy(slots).cuda())
+    if bad_slot:
+        with pytest.raises(mla.MlaError) as e:
+            mla.mla_device_error()
+        assert e.value.status == mla.MLA_ERR_DEVICE_DATA
+        slots[7] = -1                                          # what the oracle writes: the rest
+    else:
+        mla.mla_device_error()
+    got = to_host_bits(q_cat)
+    qn64 = np.transpose(mi.decode_f64(qn, dtype), (1, 0, 2))                    # [H,B,K]
+    want_lat = np.transpose(orc.bmm(qn64, mi.decode_f64(w, dtype)), (1, 0, 2))  # [B,H,L]
+    check_close(to_f64(q_cat)[:, :, :L], want_lat, dtype, "absorbed latent columns")
+    sep = poisoned((H, B, L), dtype)
+    mla.mla_absorb_q(sep, to_dev(qn, dtype).transpose(0, 1), to_dev(w, dtype))
+    torch.cuda.synchronize()
+    assert np.array_equal(np.transpose(to_host_bits(sep), (1, 0, 2)), got[:, :, :L])
+    u = np.uint16 if dtype == "bf16" else np.uint32
+    want_rope = orc.concat_q(got[:, :, :L], rope)[:, :, L:]
+    assert np.array_equal(got[:, :, L:].view(u), want_rope.view(u))
+    want_cache = orc.cache_write(fill, layer * page * E, nb, page, (n_layers * page * E, E, 1), kv, kp, slots)
+    assert np.array_equal(to_host_bits(big).reshape(-1).view(u), want_cache.view(u))
