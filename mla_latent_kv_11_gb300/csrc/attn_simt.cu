@@ -677,28 +677,46 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(
 }
 
 // A sparse query's index list, compacted: its valid slots (0 <= slot < num_rows) in listed
-// order and their count; a slot past the cache is dropped and reported. One warp a query.
-__global__ void __launch_bounds__(256) sparse_compact_kernel(const int32_t* __restrict__ idx, int64_t idx_stride,
-                                                             int topk, int B, int64_t num_rows,
-                                                             int32_t* __restrict__ out, int32_t* __restrict__ counts) {
+// order and their count; a slot past the cache is dropped and reported. One block a query:
+// each thread loads up to kPer consecutive entries at once, and a block-wide exclusive scan of
+// the per-thread counts places them, so a list costs one load round and one scan per
+// blockDim * kPer entries.
+constexpr int kCompactThreads = 256;
+constexpr int kCompactPer = 8;
+__global__ void __launch_bounds__(kCompactThreads) sparse_compact_kernel(const int32_t* __restrict__ idx,
+                                                                         int64_t idx_stride, int topk, int B,
+                                                                         int64_t num_rows, int32_t* __restrict__ out,
+                                                                         int32_t* __restrict__ counts) {
+  __shared__ int warp_tot[32];
   pdl_enter();
-  const int q = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
-  if (q >= B) return;
+  const int q = blockIdx.x;
+  if (q >= B) return;   // the whole block
   const int32_t* row = idx + (int64_t)q * idx_stride;
   int32_t* o = out + (int64_t)q * topk;
-  int n = 0;
-  for (int base = 0; base < topk; base += 32) {
-    const int t = base + lane;
-    int slot = t < topk ? row[t] : -1;
-    if (slot >= num_rows) {
-      atomicOr(&g_attn_err, kErrDeviceData);
-      slot = -1;
+  int carry = 0;
+  for (int base = 0; base < topk; base += kCompactThreads * kCompactPer) {
+    const int t0 = base + threadIdx.x * kCompactPer;
+    int v[kCompactPer];
+    int n = 0;
+#pragma unroll
+    for (int i = 0; i < kCompactPer; ++i) {
+      int slot = t0 + i < topk ? row[t0 + i] : -1;
+      if (slot >= num_rows) {
+        atomicOr(&g_attn_err, kErrDeviceData);
+        slot = -1;
+      }
+      v[i] = slot;
+      n += slot >= 0;
     }
-    const unsigned m = __ballot_sync(0xffffffffu, slot >= 0);
-    if (slot >= 0) o[n + __popc(m & ((1u << lane) - 1u))] = slot;
-    n += __popc(m);
+    int tot;
+    const int ex = block_exclusive_scan(n, warp_tot, &tot);
+    int at = carry + ex;
+#pragma unroll
+    for (int i = 0; i < kCompactPer; ++i)
+      if (v[i] >= 0) o[at++] = v[i];
+    carry += tot;
   }
-  if (lane == 0) counts[q] = n;
+  if (threadIdx.x == 0) counts[q] = carry;
 }
 
 template <typename K>
@@ -806,9 +824,8 @@ cudaError_t launch_prefill_simt(mla_dtype dt, const View3& o_lat, float* lse, co
 
 cudaError_t launch_sparse_compact(const int32_t* indices, int64_t idx_stride, int32_t topk, int32_t B,
                                   int64_t num_rows, int32_t* out, int32_t* counts, cudaStream_t st) {
-  const int blocks = (int)((B + 7) / 8);
-  return launch_k(sparse_compact_kernel, blocks, 256, 0, st, indices, idx_stride, (int)topk, (int)B, num_rows, out,
-                  counts);
+  return launch_k(sparse_compact_kernel, (int)B, kCompactThreads, 0, st, indices, idx_stride, (int)topk, (int)B,
+                  num_rows, out, counts);
 }
 
 unsigned attn_simt_errors_read_clear() {
