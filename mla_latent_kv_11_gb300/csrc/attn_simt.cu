@@ -726,6 +726,35 @@ void allow_smem(K k, size_t bytes) {
 
 }  // namespace
 
+namespace {
+// Row tiles per sequence of a prefill (ceil(query tokens / tpt), none for an empty one),
+// prefix-summed into out[0..B]: one block, a block scan per blockDim sequences.
+__global__ void __launch_bounds__(1024) prefill_items_kernel(const int32_t* __restrict__ cu_q, int B, int tpt,
+                                                             int32_t* __restrict__ out) {
+  __shared__ int warp_tot[32];
+  pdl_enter();
+  int carry = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int n = 0;
+    if (b < B) {
+      const int q = cu_q[b + 1] - cu_q[b];
+      n = q > 0 ? (q + tpt - 1) / tpt : 0;
+    }
+    int tot;
+    const int ex = block_exclusive_scan(n, warp_tot, &tot);
+    if (b < B) out[b] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) out[B] = carry;
+}
+}  // namespace
+
+cudaError_t launch_prefill_items(const int32_t* cu_q, int32_t B, int32_t tpt, int32_t* out, cudaStream_t st) {
+  const int threads = std::min(1024, std::max(32, (B + 31) / 32 * 32));
+  return launch_k(prefill_items_kernel, 1, threads, 0, st, cu_q, (int)B, (int)tpt, out);
+}
+
 cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
                                    int32_t page, const DecodeSched& s, cudaStream_t st) {
   const long long cap = (long long)max_blocks * page;

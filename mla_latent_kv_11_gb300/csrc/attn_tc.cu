@@ -1394,20 +1394,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();   // no CTA leaves while its peer may still touch its shared memory
 }
 
-// Row tiles per sequence (prefill), prefix-summed: one CTA.
-__global__ void prefill_items_kernel(const int32_t* __restrict__ cu_q, int B, int tpt, int32_t* __restrict__ out) {
-  pdl_enter();
-  if (threadIdx.x == 0 && blockIdx.x == 0) {
-    int acc = 0;
-    for (int b = 0; b < B; ++b) {
-      out[b] = acc;
-      const int q = cu_q[b + 1] - cu_q[b];
-      acc += q > 0 ? (q + tpt - 1) / tpt : 0;
-    }
-    out[B] = acc;
-  }
-}
-
 template <int kRope, int kSrc = 0>
 int max_clusters() {
   static std::mutex mu;
@@ -1664,7 +1650,7 @@ cudaError_t launch_prefill_tc(const View3& o_lat, float* lse, const View3& q, co
   p.cu_q = cu_q;
   p.kv_lens = kv_lens;
   p.item_prefix = item_prefix;
-  cudaError_t e = launch_k(prefill_items_kernel, 1, 32, 0, st, cu_q, B, p.tpt, item_prefix);
+  cudaError_t e = launch_prefill_items(cu_q, B, p.tpt, item_prefix, st);
   if (e != cudaSuccess) return e;
   const int clusters = R == 64 ? max_clusters<64, 0>() : max_clusters<0, 0>();
   return run_tc(MLA_BF16, p, q, cache, clusters, st);

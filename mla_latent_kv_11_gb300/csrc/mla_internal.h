@@ -132,6 +132,8 @@ cudaError_t launch_bmm_simt(mla_dtype dt, const View3& out, const View3& a, cons
 bool bmm_tc_supported(mla_dtype dt, const View3& out, const View3& a, const View3& b);
 cudaError_t launch_bmm_tc(const View3& out, const View3& a, const View3& b, cudaStream_t st);
 
+// Row tiles per prefill sequence, prefix-summed into out[0..B] (one block).
+cudaError_t launch_prefill_items(const int32_t* cu_q, int32_t B, int32_t tpt, int32_t* out, cudaStream_t st);
 cudaError_t launch_decode_schedule(const int32_t* seq_lens, int32_t B, int32_t max_blocks,
                                    int32_t page, const DecodeSched& s, cudaStream_t st);
 // fp8_cache: the cache holds e4m3 codes (one byte each), read as value * (*descale_k) with the
