@@ -505,13 +505,16 @@ template <typename T>
 __global__ void __launch_bounds__(128) decode_combine_kernel(
     T* __restrict__ o_lat, int64_t o_s0, int64_t o_s1, float* __restrict__ lse_out,
     int B, int H, int L, DecodeSched s) {
-  pdl_enter();
   const int b = blockIdx.x;
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (h >= H) return;
+  // a sequence's piece count and first slot come from the schedule kernel two launches back,
+  // complete before this kernel can launch (the split kernel between waits for it before it
+  // lets dependents launch): read before this kernel's wait; the partials only after it
   const int np = s.npieces[b];
   const int base = s.piece_base[b];   // loaded beside np: one memory latency for both
   if (np == 1) return;
+  pdl_enter();
   T* o = o_lat + (int64_t)b * o_s0 + (int64_t)h * o_s1;
   if (np == 0) {
     for (int c = lane; c < L; c += 32) st(o + c, 0.f);
