@@ -756,29 +756,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         while (ok && wk.next(p, sg)) {
           const int nt = ntiles(sg);
+          // the block id (pages) or slot (ds_mla) of this lane's rows lane and lane + 32 of a
+          // tile; the next tile's are loaded while this one's copies are issued
+          auto fetch = [&](int jj, int (&raw)[2]) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int t = sg.k0 + jj * kKeysT + lane + 32 * k;
+              raw[k] = t >= sg.k1 ? -1
+                       : kSrc == 1 ? p.block_table[(int64_t)sg.b * p.bt_stride + t / p.page]
+                                   : p.slots[(int64_t)sg.b * p.slot_stride + t];   // compacted: in range
+            }
+          };
+          int raw[2], nxt[2] = {-1, -1};
+          if (nt > 0) fetch(0, raw);
           for (int j = 0; ok && j < nt; ++j, ++gi) {
             const int u = gi % C::kStg;
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.stg_empty[u], ((gi / C::kStg) & 1) ^ 1, abort));
             if (!ok) break;
+            if (j + 1 < nt) fetch(j + 1, nxt);
             // byte offset of each row of the tile (-1: past the segment or a bad block id)
             int64_t* rb = rowbase + (gi & 1) * kKeysT;
-            for (int r = lane; r < kKeysT; r += 32) {
-              const int t = sg.k0 + j * kKeysT + r;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int r = lane + 32 * k, t = sg.k0 + j * kKeysT + r;
               int64_t off = -1;
               if (t < sg.k1) {
                 if (kSrc == 1) {
-                  const int blk = p.block_table[(int64_t)sg.b * p.bt_stride + t / p.page];
+                  const int blk = raw[k];
                   if (blk >= 0 && blk < p.num_blocks)
                     off = (int64_t)blk * p.s_blk8 + (int64_t)(t % p.page) * p.s_row8;
                   else
                     atomicOr(&g_tc_err, kErrDeviceData);
                 } else {
-                  const int slot = p.slots[(int64_t)sg.b * p.slot_stride + t];   // compacted: in range
+                  const int slot = raw[k];
                   off = (int64_t)(slot / p.page) * p.s_blk8 + (int64_t)(slot % p.page) * p.s_row8;
                 }
               }
               rb[r] = off;
             }
+            raw[0] = nxt[0];
+            raw[1] = nxt[1];
             __syncwarp();
             const uint32_t dst0 = smem_u32(stg + u * C::kStgBytes);
             // the 16 latent granules of every row, then the tail granules (rope; and the scales
