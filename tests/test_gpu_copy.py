@@ -222,7 +222,7 @@ def test_concat_and_cache_write_in_one_launch_edges(mla, dtype, case):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("case", FUSED_CASES, ids=["v3_b64", "v2lite_bcast", "odd"])
+@pytest.mark.parametrize("case", FUSED_CASES + [(64, 6, 256, 512, 0, 64)], ids=["v3_b64", "v2lite_bcast", "odd", "nope_h64"])
 @pytest.mark.parametrize("bad_slot", [False, True], ids=["slots_ok", "slot_past_cache"])
 def test_absorb_concat_cache_write_in_one_call(mla, dtype, case, bad_slot):
     # Steps 1 to 3 in one call (the copies alongside the absorb): the latent columns of q_cat
