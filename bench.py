@@ -675,6 +675,8 @@ def component_figures(mla, mi, device, only=None) -> dict:
         prefill_figures(mla, mi, device, out, peaks, timed)
     if want("decode"):
         decode_figures(mla, mi, device, out, peaks, timed)
+    if want("decode") or want("sparse"):
+        sparse_figures(mla, mi, device, out, peaks, timed)
     if want("copy"):
         copy_figures(mla, mi, device, out, peaks, dev, device_timed, l2_bytes)
     return out
@@ -737,11 +739,17 @@ def decode_figures(mla, mi, device, out, peaks, timed) -> None:
             nbytes8 = decode_algorithmic_bytes([ctx] * B, B, H, L, R, nbl, cache_es=1)
             out["decode_fp8_b64_ctx8192_fixed"] = {
                 "ms": ms8, "gbs": nbytes8 / (ms8 * 1e-3) / 1e9, "queries_per_s": B / (ms8 * 1e-3),
-                "path": "tensor cores (e4m3 rows gathered and converted to bf16 in shared memory)",
+                "path": "tensor cores (e4m3 pages loaded by TMA, converted to bf16 in shared memory)",
                 "roofline": roofline(nbytes8, flops, ms8, peaks)}
             del cache8, rows, slots
         del cache, q, o, ws
     del table, lens
+
+
+def sparse_figures(mla, mi, device, out, peaks, timed) -> None:
+    """Sparse top-2048 decode over an fp8 ds_mla cache."""
+    import numpy as np
+    import torch
     # sparse top-2048 decode over an fp8 ds_mla cache: 64 queries of 128 heads, distinct slots
     # scattered over 4096 blocks of 64 entries (172 MB), every slot list full
     nrows = 4096 * 64
@@ -823,7 +831,7 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-components", action="store_true", help="skip the per-stage figures")
-    ap.add_argument("--component", action="append", choices=["prefill", "decode", "copy"],
+    ap.add_argument("--component", action="append", choices=["prefill", "decode", "sparse", "copy"],
                     help="run only these per-stage figures (no decode step) and print them")
     args = ap.parse_args()
     if args.warmup < 3:
